@@ -1,0 +1,438 @@
+"""Benchmark of one paged-KV attention step on GB300.
+
+Default workload: Llama-2-13B-shaped MHA decode layer (64 sequences, 40/40
+heads, head_dim 128, block size 64, context lengths U[128, 4096], bf16 KV,
+1.25x pool with permuted page ids).  One step = kv_append of the batch's new
+tokens + paged decode attention over the whole batch (planner, split-K decode,
+merge).  --workload selects another configuration (1..5); configuration 5 adds
+the chunked-prefill call to the step.
+
+Prints ONE JSON line.  `value` = algorithmic bytes of the step / device time
+per step (KV bytes dominate; see the design doc for the byte count).  `e2e` is the
+same metric through the public API with inputs copied from pinned host memory
+and the output copied back inside the timed region.  --impl reference times
+the fp64 CPU oracle on a bounded sample of the same workload.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+(nothing in the step shards across GPUs); value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-steps/s per layer"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = 2
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def _src_hash(name):
+    path = os.path.join(ROOT, "paged_kv_attention_31_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:12]
+
+
+def _ncu_traffic(kernel, workload_name):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = _src_hash("decode.cu" if kernel == "decode_kernel" else "prefill.cu")
+    for line in open(path):
+        m = re.match(r"\s*-\s*traffic:\s*(\S+)\s+(\S+)\s+bytes_per_launch=(\d+)\s+src=(\w+)", line)
+        if m and m.group(1) == kernel and m.group(2) == workload_name and m.group(4) == want:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler around the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# oracle CPU baseline (test infrastructure; only this leg touches oracle/)
+# ---------------------------------------------------------------------------
+def _oracle_sample(w, seqs, gen_device):
+    """Host inputs for the oracle on decode sequences `seqs` (all heads):
+    pool pages from the seeded generator (on gen_device, bit-identical to
+    the host generator), then the oracle's own kv_append of the new tokens."""
+    import oracle
+    import workloads as W
+
+    P = w.block_size
+    pages, tables = [], []
+    for s in seqs:
+        n = (int(w.context_lens[s]) + P - 1) // P
+        tables.append(np.arange(len(pages), len(pages) + n, dtype=np.int32))
+        pages.extend(int(p) for p in w.block_tables[s, :n])
+    nb = len(pages)
+    maxb = max(len(t) for t in tables)
+    bt = np.full((len(seqs), maxb), -1, np.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    dt = np.uint16 if w.kv_dtype == "bf16" else np.uint8
+    pools = []
+    for c in ("k", "v"):
+        src = W.pool_values(w.seed, c, pages, w.num_kv_heads, P, w.head_dim, gen_device)
+        pools.append(W.bf16_bits(src))
+    kp = np.zeros((nb, w.num_kv_heads, P, w.head_dim), dt)
+    vp = np.zeros_like(kp)
+    rows = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3).reshape(nb * P, w.num_kv_heads,
+                                                                           w.head_dim))
+    oracle.kv_append(rows(pools[0]), rows(pools[1]), np.arange(nb * P, dtype=np.int64), kp, vp,
+                     w.kv_dtype, w.k_scale, w.v_scale)
+    kn, vn = w.kv_new()
+    kn, vn = W.bf16_bits(kn), W.bf16_bits(vn)
+    slots = w.decode_slot_mapping()
+    remap = {p: i for i, p in enumerate(pages)}
+    sel = [s for s in seqs if slots[s] >= 0]
+    mapped = np.array([remap[int(slots[s]) // P] * P + int(slots[s]) % P for s in sel], np.int64)
+    q = W.bf16_bits(w.q_decode())[list(seqs)]
+    return dict(q=np.ascontiguousarray(q), kp=kp, vp=vp, bt=bt,
+                cl=np.ascontiguousarray(w.context_lens[list(seqs)]),
+                kn=np.ascontiguousarray(kn[sel]), vn=np.ascontiguousarray(vn[sel]),
+                slots=mapped)
+
+
+def _oracle_step(w, inp):
+    """One oracle step on the sample: kv_append of the new tokens, attention."""
+    import oracle
+    kp, vp = inp["kp"].copy(), inp["vp"].copy()
+    t0 = time.perf_counter()
+    oracle.kv_append(inp["kn"], inp["vn"], inp["slots"], kp, vp, w.kv_dtype, w.k_scale,
+                     w.v_scale)
+    oracle.paged_attention(inp["q"], kp, vp, inp["bt"], inp["cl"], w.scale, w.kv_dtype,
+                           w.k_scale, w.v_scale)
+    return time.perf_counter() - t0
+
+
+def _sample_seqs(w, target_s):
+    """Sequences (spread over the batch) whose oracle work is about target_s."""
+    per_tok_row = 1.15e-6 * w.head_dim / 128         # seconds per (token, q head)
+    order = np.random.default_rng(0).permutation(w.num_seqs)
+    seqs, est = [], 0.0
+    for s in order:
+        seqs.append(int(s))
+        est += int(w.context_lens[s]) * w.num_q_heads * per_tok_row
+        if est >= target_s:
+            break
+    return sorted(seqs)
+
+
+def _sample_bytes(w, seqs):
+    per_tok = w.num_kv_heads * 2 * w.head_dim * w.elem_bytes
+    return int(sum(int(w.context_lens[s]) for s in seqs)) * per_tok
+
+
+def cpu_baseline(w, target_s, gen_device):
+    seqs = _sample_seqs(w, target_s)
+    inp = _oracle_sample(w, seqs, gen_device)
+    dt = _oracle_step(w, inp)
+    nbytes = _sample_bytes(w, seqs)
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(seqs)} of {w.num_seqs} sequences x all {w.num_q_heads} q heads "
+                      f"({nbytes / 1e6:.1f} MB of KV), fp64 C oracle, one thread, {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------------------
+def _workload(i):
+    import workloads as W
+    return W.config(i)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(bytes_per_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s of `world` independent replicas, timed by the slowest."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    w = _workload(args.workload)
+    seqs = _sample_seqs(w, args.ref_sample_s)
+    inp = _oracle_sample(w, seqs, "cpu")
+    for _ in range(args.warmup):
+        _oracle_step(w, inp)
+    times = [_oracle_step(w, inp) for _ in range(args.steps)]
+    nbytes = _sample_bytes(w, seqs)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: {len(seqs)} of {w.num_seqs} sequences x all "
+                                       f"{w.num_q_heads} q heads ({nbytes / 1e6:.1f} MB of KV)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def _config(w, args):
+    c = {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+         "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+         "kv_dtype": w.kv_dtype, "max_context_len": w.max_context_len,
+         "mean_context_len": float(np.mean(w.context_lens)), "num_blocks": w.num_blocks,
+         "partition_tokens": args.partition or "auto",
+         "l2": "no flush: each step streams the whole KV set, far larger than the 129 MB L2",
+         "parallelism": f"replicas x{args.gpus}"}
+    if w.num_prefill:
+        c["prefill_chunks"] = [int(x) for x in w.prefill_chunk_lens]
+    return c
+
+
+def run_gpu(args):
+    import torch
+
+    import paged_kv_attention_31_gb300 as pkv
+    from tests._gpu_state import device_pools, device_step_inputs
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = _workload(args.workload)
+    peaks, peak_kind = _peaks()
+
+    # --- inputs resident in HBM ---------------------------------------------------
+    d = device_step_inputs(w, dev)
+    kp, vp = device_pools(w, dev)
+    cpu_line = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_line = cpu_baseline(w, args.cpu_sample_s, dev)
+    B, Hq, D = w.num_seqs, w.num_q_heads, w.head_dim
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    ws_bytes = pkv.paged_attention_workspace_size(B, Hq, w.max_context_len, kp, args.partition,
+                                                  w.k_scale, w.v_scale)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    has_prefill = w.num_prefill > 0
+    if has_prefill:
+        out_p = torch.empty_like(d["q_prefill"])
+        max_q = int(w.prefill_chunk_lens.max())
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q, k_new, v_new, slots, bt, cl, ev=None):
+        pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=out,
+                            workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
+                            partition_tokens=args.partition)
+        if ev is not None:
+            ev[1].record(stream)
+        if has_prefill:
+            pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp,
+                              d["prefill_block_tables"], d["prefill_context_lens"], max_q,
+                              w.scale, out=out_p)
+
+    args_dev = (d["q"], d["k_new"], d["v_new"], d["slots"], d["block_tables"], d["context_lens"])
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize(dev)
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # --- timed region: device-resident inputs -------------------------------------
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(*args_dev, ev=evs[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+
+    # --- end to end through the public API from pinned host memory ------------------
+    host = [x.cpu().pin_memory() for x in args_dev]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_bufs = [torch.empty_like(x) for x in args_dev]
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for hb, db in zip(host, dev_bufs):
+            db.copy_(hb, non_blocking=True)
+        step(*dev_bufs)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # --- report ----------------------------------------------------------------------
+    step_bytes = w.decode_step_bytes()
+    ms = elapsed_ms / args.steps
+    value = replica_throughput(step_bytes, world, ms)
+    attn_bytes = (w.decode_kv_bytes() + 2 * B * Hq * D * 2 +
+                  int(np.sum((w.context_lens.astype(np.int64) + w.block_size - 1)
+                             // w.block_size)) * 4 + B * 4)
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,
+                                                w.k_scale, w.v_scale)
+    splits = max_splits > 1
+    launches_per_step += 1 if splits else 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 kv, bf16 q/out",
+        "data": "synthetic", "config": _config(w, args),
+        "seq_steps_per_s": world * B / (ms * 1e-3),
+        "frac_of_hbm_peak": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel (pkv_paged_attention: plan + decode + merge)",
+                     "algorithmic_bytes_per_launch": attn_bytes,
+                     "traffic": _ncu_traffic("decode_kernel", w.name)},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+    }
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--partition", type=int, default=0,
+                    help="split-K partition tokens (0 = library's automatic choice)")
+    ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--ref-sample-s", type=float, default=0.5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

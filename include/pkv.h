@@ -1,0 +1,203 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * One attention step of an in-flight-batching engine over a paged KV cache,
+ * as the page "TensorRT-LLM框架解析与高性能推理优化实践" describes it:
+ * K/V of every live sequence sit in fixed-size pages of one shared pool
+ * (§4.2 "KV缓存管理细节"), a per-sequence block table maps logical pages to
+ * physical ones (§6.2 "Paged Attention优化": block_tables
+ * [num_seqs, max_blocks]), sequences may share prefix pages (§6.2
+ * "共享前缀优化"), the KV cache may be stored quantised and is dequantised
+ * inside the attention kernel (§7.2 "KV Cache量化"), and long prompts are
+ * processed as chunks interleaved with decode requests (§5.3 "分块上下文处理").
+ *
+ * Conventions for every entry point
+ *  - Pointers named as device data are device memory owned by the caller;
+ *    descriptors (pkv_pool_desc) are host memory.  The library allocates no
+ *    memory: scratch space (workspace) is sized by a query and passed in.
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
+ *    is the legacy default stream), in stream order.  Nothing synchronises
+ *    the host except pkv_get_device_error.
+ *  - Arguments are validated on the host before anything is enqueued;
+ *    an invalid call returns an error and enqueues nothing.
+ *  - Device data (block-table entries, context lengths, slots) is not read by
+ *    the host.  Kernels check it: an out-of-range page id or slot is skipped
+ *    (never dereferenced) and recorded in a sticky per-device error word that
+ *    pkv_get_device_error returns.  Kernels never trap and every wait in them
+ *    is bounded; a wait that runs out is recorded the same way.
+ *
+ * Data layout
+ *  - KV pool: k_pool, v_pool = [num_blocks][num_kv_heads][block_size][head_dim],
+ *    row-major, element type bf16 or FP8 E4M3 (OCP OFP8).  One (page, kv head)
+ *    is a contiguous block_size*head_dim run.
+ *  - Pool slot: slot = page * block_size + offset (offset < block_size).
+ *  - GQA: q head a reads kv head a / (num_q_heads / num_kv_heads).
+ *  - context_lens[s] counts every token of sequence s INCLUDING the ones
+ *    appended in this step: append first (pkv_kv_append), then attend.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, group size, ... */
+    PKV_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE_BOUNDS = 5, /* a kernel met an out-of-range page id or slot */
+    PKV_ERR_DEVICE_TIMEOUT = 6 /* a bounded wait inside a kernel ran out */
+} pkv_status;
+
+typedef enum pkv_kv_dtype {
+    PKV_KV_BF16 = 0,
+    PKV_KV_FP8_E4M3 = 1        /* per-tensor scales: value = e4m3(code) * scale */
+} pkv_kv_dtype;
+
+/* Shape of the paged pool.  head_dim in {64, 128}; block_size in
+ * {16, 32, 64}; k_scale / v_scale (> 0, finite) are used only for FP8. */
+typedef struct pkv_pool_desc {
+    int32_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t kv_dtype;          /* pkv_kv_dtype */
+    float k_scale;
+    float v_scale;
+} pkv_pool_desc;
+
+/*
+ * pkv_kv_append -- write this step's new tokens into their pool slots.
+ * (§4.2: pages allow non-contiguous storage of a growing sequence.)
+ *
+ *   k_new, v_new   device, bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ *   slot_mapping   device, int64 [num_tokens]; token t goes to page
+ *                  slot/block_size, offset slot%block_size.  slot < 0: skipped
+ *                  (padding).  slot >= num_blocks*block_size: skipped and
+ *                  recorded as PKV_ERR_DEVICE_BOUNDS.
+ *   k_pool, v_pool device pools (see layout above), 16-byte aligned
+ *   pool           host descriptor
+ * bf16 pools store the bits unchanged.  FP8 pools store
+ * e4m3_rn_satfinite(x / scale), the quotient taken in IEEE binary32.
+ * num_tokens == 0 is a no-op.  Two tokens with the same slot race.
+ */
+PKV_API pkv_status pkv_kv_append(const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, int32_t num_tokens,
+                         void *k_pool, void *v_pool, const pkv_pool_desc *pool,
+                         void *stream);
+
+/*
+ * Bytes of workspace pkv_paged_attention needs for these sizes (0 never
+ * returned; at most a few hundred bytes per (sequence, q head, partition)).
+ * partition_tokens as for pkv_paged_attention.  Returns 0 for invalid sizes.
+ */
+PKV_API size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_context_len,
+                                          int32_t partition_tokens,
+                                          const pkv_pool_desc *pool);
+
+/*
+ * The split plan pkv_paged_attention uses for these sizes: *partition_out
+ * receives the partition length in tokens (partition_tokens if > 0, else the
+ * automatic choice) and *max_splits_out the largest number of partitions of
+ * one sequence (1 = no split, the merge kernel is not launched).  Host-only.
+ */
+PKV_API pkv_status pkv_paged_attention_plan(int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t max_context_len, int32_t partition_tokens,
+                                            const pkv_pool_desc *pool, int32_t *partition_out,
+                                            int32_t *max_splits_out);
+
+/*
+ * pkv_paged_attention -- decode attention for a batch of sequences, one
+ * query token each (§6.2 "Paged Attention优化"; running max/sum of §6.1).
+ *
+ *   out[s][a][:] = sum_i softmax_i(scale * <q[s][a], K_s[i]>) * V_s[i]
+ *   over i < context_lens[s], K_s[i] = k_pool[block_tables[s][i/P]][a/G][i%P].
+ *
+ *   q               device, bf16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
+ *   k_pool, v_pool  device pools, 16-byte aligned
+ *   block_tables    device, int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens    device, int32 [num_seqs]; each in [0, max_context_len]
+ *                   (length 0 gives a zero output row)
+ *   max_context_len host upper bound of context_lens (sizes the split plan)
+ *   scale           softmax scale (e.g. 1/sqrt(head_dim)); FP8 scores are
+ *                   additionally multiplied by k_scale and outputs by v_scale
+ *   partition_tokens split-K partition length in tokens: a sequence longer
+ *                   than it is processed as ceil(L/partition) independent
+ *                   partitions merged by a second kernel.  0 = automatic.
+ *                   Must be a multiple of block_size otherwise.
+ *   workspace       device scratch of >= pkv_paged_attention_workspace_size
+ *                   bytes, 256-byte aligned; contents need not be initialised
+ *                   and are clobbered.  Calls sharing a workspace must be
+ *                   stream-ordered.
+ *   out             device, bf16 [num_seqs][num_q_heads][head_dim]
+ * num_q_heads must be a multiple of num_kv_heads with a group size of
+ * 1, 2, 4 or 8.  num_seqs == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_paged_attention(const void *q, const void *k_pool, const void *v_pool,
+                               const pkv_pool_desc *pool, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads,
+                               int32_t max_context_len, float scale,
+                               int32_t partition_tokens, void *workspace,
+                               size_t workspace_bytes, void *out, void *stream);
+
+/*
+ * pkv_paged_prefill -- causal attention of prefill-chunk tokens over their
+ * sequences' pages (§5.3 "分块上下文处理": chunked context).
+ *
+ *   Sequence s owns packed query rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+ *   (C_s rows).  context_lens[s] = L_s counts the chunk, whose K/V must have
+ *   been appended already.  Row i of sequence s (position L_s - C_s + i)
+ *   attends to keys 0 .. L_s - C_s + i.
+ *
+ *   q               device, bf16 [num_q_tokens][num_q_heads][head_dim], 16-byte aligned
+ *   cu_seqlens_q    device, int32 [num_seqs + 1], non-decreasing, [0] = 0,
+ *                   [num_seqs] = num_q_tokens, each C_s <= min(max_q_len, L_s)
+ *   k_pool, v_pool  device pools (bf16 only), 16-byte aligned
+ *   block_tables    device, int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens    device, int32 [num_seqs]
+ *   max_q_len       host upper bound of C_s
+ *   out             device, bf16 [num_q_tokens][num_q_heads][head_dim]
+ * head_dim must be 128; the group size num_q_heads/num_kv_heads must divide
+ * 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
+ */
+PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
+                             const void *k_pool, const void *v_pool,
+                             const pkv_pool_desc *pool, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t max_q_len,
+                             int32_t num_q_tokens, float scale, void *out,
+                             void *stream);
+
+/*
+ * pkv_get_device_error -- synchronise `stream`, then read and clear the
+ * current device's sticky error word.  *code receives PKV_OK,
+ * PKV_ERR_DEVICE_BOUNDS or PKV_ERR_DEVICE_TIMEOUT (the first error recorded
+ * since the last call).  Returns PKV_ERR_CUDA if the synchronisation fails.
+ */
+PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
+
+/* Static string for a status code (never NULL). */
+PKV_API const char *pkv_status_string(int32_t status);
+
+/* Library ABI version (major * 100 + minor). */
+PKV_API int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

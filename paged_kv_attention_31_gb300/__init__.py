@@ -1,0 +1,224 @@
+"""Thin Python binding of libpkv.so, the GB300 paged-KV attention library.
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels behind the C ABI declared in include/pkv.h.  Tensors are torch CUDA
+tensors; each call is enqueued on torch's current CUDA stream.  There is no
+CPU fallback: if the compiled library is missing, importing a function raises.
+
+Functions mirror the C entry points:
+    kv_append                       <- pkv_kv_append
+    paged_attention_workspace_size  <- pkv_paged_attention_workspace_size
+    paged_attention_plan            <- pkv_paged_attention_plan
+    paged_attention                 <- pkv_paged_attention
+    paged_prefill                   <- pkv_paged_prefill
+    get_device_error                <- pkv_get_device_error
+    status_string                   <- pkv_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_DEVICE_BOUNDS = 5
+PKV_ERR_DEVICE_TIMEOUT = 6
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+def lib():
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m paged_kv_attention_31_gb300.build` (no CPU fallback exists)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                     ctypes.c_float, ctypes.c_size_t)
+            pd = ctypes.POINTER(PoolDesc)
+            L.pkv_kv_append.restype = i32
+            L.pkv_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, pd, vp]
+            L.pkv_paged_attention_workspace_size.restype = sz
+            L.pkv_paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, pd]
+            L.pkv_paged_attention_plan.restype = i32
+            L.pkv_paged_attention_plan.argtypes = [i32, i32, i32, i32, pd,
+                                                   ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.pkv_paged_attention.restype = i32
+            L.pkv_paged_attention.argtypes = [vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, f32,
+                                              i32, vp, sz, vp, vp]
+            L.pkv_paged_prefill.restype = i32
+            L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, i32,
+                                            f32, vp, vp]
+            L.pkv_get_device_error.restype = i32
+            L.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
+            L.pkv_status_string.restype = ctypes.c_char_p
+            L.pkv_status_string.argtypes = [i32]
+            L.pkv_version.restype = i32
+            L.pkv_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _is_fp8_pool(pool: torch.Tensor) -> bool:
+    if pool.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return True
+    if pool.dtype == torch.bfloat16:
+        return False
+    raise TypeError("pool must be bfloat16, uint8 or float8_e4m3fn")
+
+
+def pool_desc(k_pool: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> PoolDesc:
+    """Descriptor of a pool tensor [num_blocks, Hkv, block_size, head_dim]."""
+    if k_pool.dim() != 4:
+        raise ValueError("pool must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hkv, P, D = k_pool.shape
+    return PoolDesc(nb, hkv, P, D, KV_FP8_E4M3 if _is_fp8_pool(k_pool) else KV_BF16,
+                    float(k_scale), float(v_scale))
+
+
+def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale=1.0, v_scale=1.0,
+              stream=None) -> None:
+    """Write new tokens' K/V rows ([T, Hkv, D] bf16) to their pool slots."""
+    if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16:
+        raise TypeError("k_new / v_new must be bfloat16")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    if v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("k_pool and v_pool differ")
+    T = int(slot_mapping.shape[0])
+    if tuple(k_new.shape) != (T, desc.num_kv_heads, desc.head_dim) or k_new.shape != v_new.shape:
+        raise ValueError("k_new / v_new must be [T, num_kv_heads, head_dim]")
+    _check(lib().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(k_pool),
+                               _ptr(v_pool), ctypes.byref(desc), _stream(stream)),
+           "pkv_kv_append")
+
+
+def paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len, k_pool,
+                                   partition_tokens=0, k_scale=1.0, v_scale=1.0) -> int:
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    n = lib().pkv_paged_attention_workspace_size(int(num_seqs), int(num_q_heads),
+                                                 int(max_context_len), int(partition_tokens),
+                                                 ctypes.byref(desc))
+    if n == 0:
+        raise ValueError("invalid sizes for pkv_paged_attention_workspace_size")
+    return int(n)
+
+
+def paged_attention_plan(num_seqs, num_q_heads, max_context_len, k_pool, partition_tokens=0,
+                         k_scale=1.0, v_scale=1.0):
+    """(partition_tokens, max_splits) that paged_attention will use."""
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    part, splits = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().pkv_paged_attention_plan(int(num_seqs), int(num_q_heads), int(max_context_len),
+                                          int(partition_tokens), ctypes.byref(desc),
+                                          ctypes.byref(part), ctypes.byref(splits)),
+           "pkv_paged_attention_plan")
+    return int(part.value), int(splits.value)
+
+
+def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale,
+                    out=None, workspace=None, k_scale=1.0, v_scale=1.0, partition_tokens=0,
+                    stream=None) -> torch.Tensor:
+    """Decode attention: q [B, Hq, D] bf16 -> out [B, Hq, D] bf16."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3:
+        raise TypeError("q must be bfloat16 [num_seqs, num_q_heads, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables / context_lens must be int32")
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool,
+                                                partition_tokens, k_scale, v_scale)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(lib().pkv_paged_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), ctypes.byref(desc),
+                                     _ptr(block_tables), int(block_tables.shape[1]),
+                                     _ptr(context_lens), int(B), int(Hq), int(max_context_len),
+                                     float(scale), int(partition_tokens), _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()),
+                                     _ptr(out), _stream(stream)),
+           "pkv_paged_attention")
+    return out
+
+
+def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens, max_q_len,
+                  scale, out=None, stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention: q [T, Hq, D] bf16 -> out [T, Hq, D] bf16."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3:
+        raise TypeError("q must be bfloat16 [num_q_tokens, num_q_heads, head_dim]")
+    for t in (cu_seqlens_q, block_tables, context_lens):
+        if t.dtype != torch.int32:
+            raise TypeError("cu_seqlens_q / block_tables / context_lens must be int32")
+    desc = pool_desc(k_pool)
+    T, Hq, D = q.shape
+    n = int(context_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().pkv_paged_prefill(_ptr(q), _ptr(cu_seqlens_q), _ptr(k_pool), _ptr(v_pool),
+                                   ctypes.byref(desc), _ptr(block_tables),
+                                   int(block_tables.shape[1]), _ptr(context_lens), n, int(Hq),
+                                   int(max_q_len), int(T), float(scale), _ptr(out),
+                                   _stream(stream)),
+           "pkv_paged_prefill")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise, then read and clear the device's sticky error word."""
+    code = ctypes.c_int32(0)
+    _check(lib().pkv_get_device_error(ctypes.byref(code), _stream(stream)),
+           "pkv_get_device_error")
+    return int(code.value)

@@ -1,0 +1,311 @@
+// pkv_api.cu -- the C ABI of include/pkv.h: host-side validation, split
+// planning and kernel dispatch.  No allocation happens here; every kernel is
+// enqueued on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include "pkv_common.cuh"
+#include "pkv_launch.h"
+
+// Sticky per-device error word written by the kernels (first error wins).
+__device__ int32_t g_pkv_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int32_t* err = nullptr;
+  bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+pkv_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    void* addr = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (cudaGetSymbolAddress(&addr, g_pkv_device_error) != cudaSuccess) return PKV_ERR_CUDA;
+    d.num_sms = sms;
+    d.err = static_cast<int32_t*>(addr);
+    d.ready = true;
+  }
+  *out = &d;
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+pkv_status check_pool(const pkv_pool_desc* pool) {
+  if (!pool) return PKV_ERR_INVALID_ARG;
+  if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (pool->kv_dtype != PKV_KV_BF16 && pool->kv_dtype != PKV_KV_FP8_E4M3)
+    return PKV_ERR_INVALID_ARG;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (pool->block_size != 16 && pool->block_size != 32 && pool->block_size != 64)
+    return PKV_ERR_UNSUPPORTED;
+  if (pool->kv_dtype == PKV_KV_FP8_E4M3) {
+    if (!(pool->k_scale > 0.f) || !(pool->v_scale > 0.f) || !isfinite(pool->k_scale) ||
+        !isfinite(pool->v_scale))
+      return PKV_ERR_INVALID_ARG;
+  }
+  return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return PKV_ERR_CUDA;
+}
+
+// Split-K partition length: explicit (validated) or automatic.  The automatic
+// choice keeps the largest work unit (one kv head of one partition) at about
+// 1/8 of one CTA's share of an estimated total (half the maximum context per
+// sequence), so the longest-first dynamic schedule stays balanced; never below
+// 512 tokens, and no split when every sequence fits in one unit anyway.
+int choose_partition(int32_t requested, int num_seqs, int num_kv_heads, int max_len,
+                     int block_size, int elem_bytes, int head_dim, int num_sms) {
+  if (requested > 0) return requested;
+  const double per_tok = 2.0 * head_dim * elem_bytes;  // K+V bytes per token per kv head
+  const double total = double(num_seqs) * num_kv_heads * (max_len / 2.0 + 1) * per_tok;
+  const double per_cta = total / (double(num_sms) * 2.0);
+  double tok = per_cta / 8.0 / per_tok;
+  int part = 512;
+  while (part * 2 <= tok && part < 8192) part *= 2;
+  if (part >= max_len) part = ((max_len + block_size - 1) / block_size) * block_size;
+  if (part < block_size) part = block_size;
+  part = (part / block_size) * block_size;
+  return part;
+}
+
+pkv_status validate_partition(int32_t partition, int block_size) {
+  if (partition < 0) return PKV_ERR_INVALID_ARG;
+  if (partition > 0 && (partition % block_size != 0 || partition > 16368))
+    return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_version(void) { return 100; }
+
+const char* pkv_status_string(int32_t s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_BOUNDS: return "device data out of range (page id, slot or length)";
+    case PKV_ERR_DEVICE_TIMEOUT: return "bounded wait in a kernel ran out";
+    default: return "unknown status";
+  }
+}
+
+pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* k_pool, void* v_pool,
+                         const pkv_pool_desc* pool, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
+    return PKV_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  pkv::AppendParams p;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slot_mapping = slot_mapping;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.num_slots = int64_t(pool->num_blocks) * pool->block_size;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.block_size = pool->block_size;
+  p.head_dim = pool->head_dim;
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
+  p.err = dev->err;
+  return from_cuda(pkv::launch_kv_append(p, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_context_len, int32_t partition_tokens,
+                                          const pkv_pool_desc* pool) {
+  if (check_pool(pool) != PKV_OK || num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0)
+    return 0;
+  if (validate_partition(partition_tokens, pool->block_size) != PKV_OK) return 0;
+  DeviceInfo* dev = nullptr;
+  int sms = 152;
+  if (device_info(&dev) == PKV_OK) sms = dev->num_sms;
+  const int eb = pool->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+  const int part = choose_partition(partition_tokens, num_seqs, pool->num_kv_heads,
+                                    max_context_len, pool->block_size, eb, pool->head_dim, sms);
+  const int splits = pkv::decode_num_splits(max_context_len, part);
+  return pkv::decode_workspace_layout(num_seqs, num_q_heads, pool->head_dim, splits).total;
+}
+
+pkv_status pkv_paged_attention_plan(int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_context_len, int32_t partition_tokens,
+                                   const pkv_pool_desc* pool, int32_t* partition_out,
+                                   int32_t* max_splits_out) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (!partition_out || !max_splits_out || num_seqs < 0 || num_q_heads <= 0 ||
+      max_context_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if ((st = validate_partition(partition_tokens, pool->block_size)) != PKV_OK) return st;
+  DeviceInfo* dev = nullptr;
+  int sms = 152;
+  if (device_info(&dev) == PKV_OK) sms = dev->num_sms;
+  const int eb = pool->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+  const int part = choose_partition(partition_tokens, num_seqs, pool->num_kv_heads,
+                                    max_context_len, pool->block_size, eb, pool->head_dim, sms);
+  *partition_out = part;
+  *max_splits_out = pkv::decode_num_splits(max_context_len, part);
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attention(const void* q, const void* k_pool, const void* v_pool,
+                               const pkv_pool_desc* pool, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                               float scale, int32_t partition_tokens, void* workspace,
+                               size_t workspace_bytes, void* out, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / pool->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if ((st = validate_partition(partition_tokens, pool->block_size)) != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || !workspace)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3))
+    return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+
+  const bool fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
+  const int eb = fp8 ? 1 : 2;
+  const int64_t cap64 = int64_t(max_blocks_per_seq) * pool->block_size;
+  const int max_len = int(cap64 < max_context_len ? cap64 : max_context_len);
+  // the plan is chosen from the caller's max_context_len exactly as the
+  // workspace query does; the clamped max_len can only lower the split count
+  const int part = choose_partition(partition_tokens, num_seqs, pool->num_kv_heads,
+                                    max_context_len, pool->block_size, eb, pool->head_dim,
+                                    dev->num_sms);
+  const int splits = pkv::decode_num_splits(max_len, part);
+  const pkv::DecodeWorkspace ws =
+      pkv::decode_workspace_layout(num_seqs, num_q_heads, pool->head_dim, splits);
+  if (workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  pkv::DecodeParams p;
+  p.q = q;
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.counters = reinterpret_cast<int32_t*>(w + ws.counters);
+  p.items = reinterpret_cast<int2*>(w + ws.items);
+  p.ws_ml = reinterpret_cast<float*>(w + ws.ml);
+  p.ws_acc = reinterpret_cast<float*>(w + ws.acc);
+  p.err = dev->err;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.head_dim = pool->head_dim;
+  p.block_size = pool->block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = pool->num_blocks;
+  p.max_len = max_len;
+  p.partition = part;
+  p.max_splits = splits;
+  p.q_mult = scale * (fp8 ? pool->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_mult = fp8 ? pool->v_scale : 1.0f;
+  return from_cuda(pkv::launch_decode(p, fp8, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const void* k_pool,
+                             const void* v_pool, const pkv_pool_desc* pool,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t max_q_len, int32_t num_q_tokens, float scale, void* out,
+                             void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (pool->kv_dtype != PKV_KV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || num_q_tokens < 0 ||
+      max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / pool->num_kv_heads;
+  if (G > 128 || 128 % G != 0) return PKV_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_q_tokens == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !cu_seqlens_q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3))
+    return PKV_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  pkv::PrefillParams p;
+  p.q = q;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = dev->err;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.head_dim = pool->head_dim;
+  p.block_size = pool->block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = pool->num_blocks;
+  p.num_q_tokens = num_q_tokens;
+  p.tiles_per_seq = (int)((int64_t(max_q_len) * G + 127) / 128);
+  p.q_mult = scale * 1.4426950408889634f;
+  return from_cuda(
+      pkv::launch_prefill(p, k_pool, v_pool, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_get_device_error(int32_t* code, void* stream) {
+  if (!code) return PKV_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  const int32_t zero = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_pkv_device_error, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_pkv_device_error, &zero, sizeof(zero)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  *code = v;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// pkv_launch.h -- kernel parameter blocks and launchers (internal; host and
+// device code of the library include it, the public ABI is include/pkv.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct AppendParams {
+  const void* k_new;            // bf16 [T][Hkv][D]
+  const void* v_new;
+  const int64_t* slot_mapping;  // [T]
+  void* k_pool;
+  void* v_pool;
+  int64_t num_slots;            // num_blocks * block_size
+  int32_t num_tokens, num_kv_heads, block_size, head_dim;
+  float k_scale, v_scale;
+  int32_t fp8;
+  int32_t* err;
+};
+
+// Work item of the split-K decode: (sequence, partition index).
+struct DecodeParams {
+  const void* q;                // bf16 [B][Hq][D]
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* context_lens;  // [B]
+  void* out;                    // bf16 [B][Hq][D]
+  float* ws_acc;                // [B][Hq][max_splits][D], unnormalised
+  float* ws_ml;                 // [B][Hq][max_splits][2]: running max (log2), sum
+  int2* items;                  // [B * max_splits] from the planner
+  int32_t* counters;            // [0] item count, [1] work-fetch counter
+  int32_t* err;
+  int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  int32_t max_blocks, num_blocks;
+  int32_t max_len;              // effective cap on context lengths
+  int32_t partition;            // tokens per split partition (multiple of block_size)
+  int32_t max_splits;
+  float q_mult;                 // scale * k_scale * log2(e)
+  float v_mult;                 // v_scale (FP8) or 1
+};
+
+struct PrefillParams {
+  const void* q;                // bf16 [Tq][Hq][D]
+  const int32_t* cu_seqlens_q;  // [n + 1]
+  const int32_t* block_tables;  // [n][max_blocks]
+  const int32_t* context_lens;  // [n]
+  void* out;                    // bf16 [Tq][Hq][D]
+  int32_t* err;
+  int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  int32_t max_blocks, num_blocks, num_q_tokens;
+  int32_t tiles_per_seq;        // ceil(max_q_len * G / 128)
+  float q_mult;                 // scale * log2(e)
+};
+
+// Split plan shared by the host (workspace sizing) and the kernels.
+__host__ __device__ inline int decode_num_splits(int len, int partition) {
+  return len <= partition ? 1 : (len + partition - 1) / partition;
+}
+
+// Workspace layout of pkv_paged_attention (byte offsets, 256-aligned).
+struct DecodeWorkspace {
+  size_t counters, items, ml, acc, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
+                                               int max_splits) {
+  DecodeWorkspace w;
+  const size_t rows = size_t(num_seqs) * num_q_heads * max_splits;
+  w.counters = 0;
+  w.items = align256(w.counters + 4 * sizeof(int32_t));
+  w.ml = align256(w.items + size_t(num_seqs) * max_splits * 8);
+  w.acc = align256(w.ml + rows * 2 * sizeof(float));
+  w.total = align256(w.acc + rows * head_dim * sizeof(float));
+  return w;
+}
+
+cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+// Returns cudaErrorNotSupported for shapes without a kernel instance.
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
+                           int num_sms, cudaStream_t stream);
+
+}  // namespace pkv

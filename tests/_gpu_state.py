@@ -1,0 +1,126 @@
+"""GPU-test helpers: device inputs from the seeded generator, and the
+oracle-side state of one (sequence, kv head) rebuilt on the host from the
+same generator (never from the CUDA path).
+"""
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_attention_31_gb300 as pkv
+import workloads as W
+
+BF16_MAX_ABS, BF16_MEAN_ABS, FP8_MAX_ABS = 2e-2, 2e-3, 6e-2
+
+
+def device_pools(w: W.Workload, device="cuda"):
+    """Pools holding the generator's values (FP8: encoded by pkv_kv_append)."""
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    if w.kv_dtype == "bf16":
+        k = W.fill_pool_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, "k")
+        v = W.fill_pool_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, "v")
+        return k, v
+    k = torch.empty(shape, dtype=torch.uint8, device=device)
+    v = torch.empty(shape, dtype=torch.uint8, device=device)
+    per_page = w.num_kv_heads * w.block_size * w.head_dim
+    chunk = max(1, (1 << 25) // per_page)
+    P = w.block_size
+    for start in range(0, w.num_blocks, chunk):
+        stop = min(w.num_blocks, start + chunk)
+        ids = np.arange(start, stop)
+        rows = lambda x: x.permute(0, 2, 1, 3).reshape(-1, w.num_kv_heads, w.head_dim).contiguous()
+        kn = rows(w.pool_source("k", ids, device))
+        vn = rows(w.pool_source("v", ids, device))
+        slots = torch.arange(start * P, stop * P, dtype=torch.int64, device=device)
+        pkv.kv_append(kn, vn, slots, k, v, w.k_scale, w.v_scale)
+    return k, v
+
+
+def device_step_inputs(w: W.Workload, device="cuda"):
+    d = {}
+    d["q"] = w.q_decode(device)
+    d["k_new"], d["v_new"] = w.kv_new(device)
+    d["slots"] = torch.from_numpy(w.append_slot_mapping()).to(device)
+    d["block_tables"] = torch.from_numpy(w.block_tables).to(device)
+    d["context_lens"] = torch.from_numpy(w.context_lens).to(device)
+    if w.num_prefill:
+        d["q_prefill"] = w.q_prefill(device)
+        d["cu_seqlens_q"] = torch.from_numpy(w.cu_seqlens_q()).to(device)
+        d["prefill_block_tables"] = torch.from_numpy(w.prefill_block_tables).to(device)
+        d["prefill_context_lens"] = torch.from_numpy(w.prefill_context_lens).to(device)
+    return d
+
+
+def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None):
+    """Oracle pools [n, 1, P, D] for kv head h of the given pages, after this
+    step's appends: the generator's values, then oracle.kv_append of every
+    appended token whose slot falls in these pages."""
+    page_ids = np.asarray(page_ids, np.int64)
+    P, D = w.block_size, w.head_dim
+    n = len(page_ids)
+    src = {c: W.bf16_bits(W.pool_values_head(w.seed, c, page_ids, h, w.num_kv_heads, P, D))
+           for c in ("k", "v")}
+    dt = np.uint16 if w.kv_dtype == "bf16" else np.uint8
+    kp = np.zeros((n, 1, P, D), dt)
+    vp = np.zeros((n, 1, P, D), dt)
+    # initial contents: every slot of these pages
+    oracle.kv_append(src["k"].reshape(n * P, 1, D), src["v"].reshape(n * P, 1, D),
+                     np.arange(n * P, dtype=np.int64), kp, vp, w.kv_dtype, w.k_scale, w.v_scale)
+    # this step's appends that land in these pages
+    slots = w.append_slot_mapping()
+    if k_new_h is None:
+        kn, vn = w.kv_new()
+        k_new_h = W.bf16_bits(kn[:, h, :])
+        v_new_h = W.bf16_bits(vn[:, h, :])
+    where = {int(p): i for i, p in enumerate(page_ids)}
+    sel = [t for t in range(len(slots)) if int(slots[t]) // P in where]
+    if sel:
+        sel = np.array(sel)
+        mapped = np.array([where[int(slots[t]) // P] * P + int(slots[t]) % P for t in sel], np.int64)
+        oracle.kv_append(k_new_h[sel][:, None, :], v_new_h[sel][:, None, :], mapped, kp, vp,
+                         w.kv_dtype, w.k_scale, w.v_scale)
+    return kp, vp
+
+
+def oracle_decode_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
+    """fp64 oracle output [G, D] of decode sequence s, q heads of kv head h."""
+    L = int(w.context_lens[s])
+    P = w.block_size
+    npg = (L + P - 1) // P
+    pages = w.block_tables[s, :npg]
+    kp, vp = host_head_pools(w, pages, h, *(kv_new_h or (None, None)))
+    G = w.group
+    q = W.bf16_bits(w.q_decode()[s, h * G:(h + 1) * G, :])[None]
+    table = np.arange(max(npg, 1), dtype=np.int32)[None]
+    out = oracle.paged_attention(q, kp, vp, table, np.array([L], np.int32), w.scale,
+                                 w.kv_dtype, w.k_scale, w.v_scale)
+    return out[0]
+
+
+def oracle_prefill_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
+    """fp64 oracle output [C, G, D] of prefill sequence s, q heads of kv head h."""
+    L = int(w.prefill_context_lens[s])
+    C = int(w.prefill_chunk_lens[s])
+    P = w.block_size
+    npg = (L + P - 1) // P
+    pages = w.prefill_block_tables[s, :npg]
+    kp, vp = host_head_pools(w, pages, h, *(kv_new_h or (None, None)))
+    G = w.group
+    cu = w.cu_seqlens_q()
+    q = W.bf16_bits(w.q_prefill()[cu[s]:cu[s + 1], h * G:(h + 1) * G, :])
+    table = np.arange(max(npg, 1), dtype=np.int32)[None]
+    out = oracle.paged_prefill(q, np.array([0, C], np.int32), kp, vp, table,
+                               np.array([L], np.int32), w.scale)
+    return out
+
+
+def assert_close(got_bf16: torch.Tensor, want: np.ndarray, fp8: bool, what=""):
+    got = got_bf16.detach().float().cpu().numpy().astype(np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    if fp8:
+        assert err.max() <= FP8_MAX_ABS, f"{what}: max abs err {err.max():.3g}"
+    else:
+        assert err.max() <= BF16_MAX_ABS, f"{what}: max abs err {err.max():.3g}"
+        assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3g}"
+    return float(err.max()), float(err.mean())

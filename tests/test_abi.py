@@ -1,0 +1,99 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+that include/pkv.h declares.  Host-side argument validation is exercised with
+invalid arguments only (it returns before any CUDA call), so no GPU is needed.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_31_gb300 as pkv
+from paged_kv_attention_31_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("pkv_kv_append", "pkv_paged_attention", "pkv_paged_attention_workspace_size",
+              "pkv_paged_prefill", "pkv_get_device_error", "pkv_status_string", "pkv_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert lib.pkv_version() == 100
+
+
+def test_internal_symbols_hidden(lib):
+    with pytest.raises(AttributeError):
+        getattr(lib, "_ZN3pkv16launch_kv_appendERKNS_12AppendParamsEiP11CUstream_st")
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert pkv.status_string(s)
+    assert pkv.status_string(99) == "unknown status"
+
+
+def _desc(**kw):
+    d = dict(num_blocks=8, num_kv_heads=2, block_size=16, head_dim=128, kv_dtype=0,
+             k_scale=1.0, v_scale=1.0)
+    d.update(kw)
+    return pkv.PoolDesc(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), 2), (dict(block_size=8), 2), (dict(kv_dtype=7), 1),
+    (dict(num_blocks=0), 1), (dict(kv_dtype=1, k_scale=0.0), 1),
+    (dict(kv_dtype=1, v_scale=float("nan")), 1)])
+def test_pool_validation(lib, kw, status):
+    d = _desc(**kw)
+    z = ctypes.c_void_p(0)
+    assert lib.pkv_kv_append(z, z, z, 4, z, z, ctypes.byref(d), z) == status
+
+
+def test_argument_validation_before_any_cuda_call(lib):
+    d = _desc()
+    z = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(258)
+    # null pointers
+    assert lib.pkv_kv_append(z, z, z, 4, z, z, ctypes.byref(d), z) == 1
+    # misaligned pool
+    assert lib.pkv_kv_append(one, one, one, 4, odd, one, ctypes.byref(d), z) == 1
+    assert lib.pkv_kv_append(z, z, z, 0, z, z, ctypes.byref(d), z) == 0  # no-op
+    assert lib.pkv_kv_append(z, z, z, -1, z, z, ctypes.byref(d), z) == 1
+    # group size 3 unsupported, Hq not a multiple of Hkv invalid
+    args = lambda hq, part=0, ws=one: (one, one, one, ctypes.byref(d), one, 4, one, 2, hq, 100,
+                                       0.1, part, ws, 1 << 20, one, z)
+    assert lib.pkv_paged_attention(*args(6)) == 2
+    assert lib.pkv_paged_attention(*args(3)) == 1
+    assert lib.pkv_paged_attention(*args(4, part=24)) == 1     # not a multiple of block size
+    assert lib.pkv_paged_attention(*args(4, ws=ctypes.c_void_p(272))) == 3  # misaligned workspace
+    # prefill: FP8 pools and head_dim 64 are not built
+    d8 = _desc(kv_dtype=1)
+    assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d8), one, 4, one, 1, 4, 16, 16,
+                                 0.1, one, z) == 2
+    d64 = _desc(head_dim=64)
+    assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d64), one, 4, one, 1, 4, 16, 16,
+                                 0.1, one, z) == 2
+
+
+def test_workspace_size_is_positive(lib):
+    d = _desc()
+    assert lib.pkv_paged_attention_workspace_size(4, 8, 1000, 0, ctypes.byref(d)) > 0
+    assert lib.pkv_paged_attention_workspace_size(4, 8, 1000, 24, ctypes.byref(d)) == 0

@@ -1,0 +1,107 @@
+"""Chunked-prefill attention (tcgen05 kernel) on the GPU against the oracle.
+
+Tolerance as for bf16 decode: max |err| <= 2e-2, mean |err| <= 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_31_gb300 as pkv
+import workloads as W
+from tests._gpu_state import (assert_close, device_pools, device_step_inputs,
+                              oracle_decode_rows, oracle_prefill_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(w, d, kp, vp, append=True):
+    if append:
+        pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp)
+    return pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp,
+                             d["prefill_block_tables"], d["prefill_context_lens"],
+                             int(w.prefill_chunk_lens.max()), w.scale)
+
+
+def _check(w, out, seqs=None, heads=None):
+    G = w.group
+    cu = w.cu_seqlens_q()
+    kn, vn = w.kv_new()
+    for s in (range(w.num_prefill) if seqs is None else seqs):
+        for h in (range(w.num_kv_heads) if heads is None else heads):
+            kv = (W.bf16_bits(kn[:, h, :]), W.bf16_bits(vn[:, h, :]))
+            want = oracle_prefill_rows(w, s, h, kv)
+            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, False,
+                         f"{w.name} s={s} h={h}")
+
+
+def test_small_mixed_config_every_row():
+    w = W.small_config(5)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check(w, out)
+
+
+@pytest.mark.parametrize("G,P", [(1, 16), (2, 32), (4, 32), (8, 64), (4, 16), (16, 64)])
+def test_groups_blocks_and_ragged_chunks(G, P):
+    # chunks of 1 token, whole-prompt chunks (prior 0), tails that end
+    # mid-tile and mid-key-block
+    priors = [0, 7, 64, 129, 0]
+    chunks = [1, 33, 200, 64, 257]
+    hkv = 2
+    w = W.make_mixed(f"prefill_G{G}_P{P}", 900 + G + P, [40], priors, chunks, hkv * G, hkv,
+                     128, P)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check(w, out)
+
+
+def test_never_written_slots_past_the_end_do_not_leak():
+    # fill everything past each sequence's last token with NaN bit patterns
+    w = W.make_mixed("prefill_nan_tail", 1234, [30], [5, 70], [50, 27], 32, 8, 128, 32)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    P = w.block_size
+    for s in range(w.num_prefill):
+        L = int(w.prefill_context_lens[s])
+        last = int(w.prefill_block_tables[s, (L - 1) // P])
+        off = L % P
+        if off:
+            kp[last, :, off:, :] = float("nan")
+            vp[last, :, off:, :] = float("nan")
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    assert torch.isfinite(out.float()).all()
+    _check(w, out)
+
+
+def test_bad_page_id_reported():
+    w = W.small_config(5)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    d["prefill_block_tables"] = d["prefill_block_tables"].clone()
+    d["prefill_block_tables"][0, 1] = w.num_blocks + 5
+    _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_BOUNDS
+
+
+def test_full_size_mixed_step_sampled():
+    w = W.config(5)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp)
+    out_d = pkv.paged_attention(d["q"], kp, vp, d["block_tables"], d["context_lens"],
+                                w.max_context_len, w.scale)
+    out_p = _prefill(w, d, kp, vp, append=False)
+    assert pkv.get_device_error() == 0
+    G = w.group
+    rng = np.random.default_rng(5)
+    for s in range(w.num_prefill):
+        _check(w, out_p, seqs=[s], heads=[int(rng.integers(0, w.num_kv_heads))])
+    for s in (0, int(np.argmax(w.context_lens))):
+        h = int(rng.integers(0, w.num_kv_heads))
+        assert_close(out_d[s, h * G:(h + 1) * G], oracle_decode_rows(w, s, h), False,
+                     f"mixed decode s={s}")

@@ -108,10 +108,23 @@ def pool_values(seed: int, which: str, page_ids, num_kv_heads: int,
     return out.reshape(len(pages), num_kv_heads, block_size, head_dim)
 
 
+def pool_values_head(seed: int, which: str, page_ids, head: int, num_kv_heads: int,
+                     block_size: int, head_dim: int, device="cpu") -> torch.Tensor:
+    """bf16 [len(page_ids), P, D]: the kv-head ``head`` slice of pool pages."""
+    pages = torch.as_tensor(np.asarray(page_ids, dtype=np.int64), device=device)
+    run = block_size * head_dim
+    inner = torch.arange(run, dtype=torch.int64, device=device)
+    idx = (pages[:, None] * num_kv_heads + head) * run + inner[None, :]
+    out = normal_bf16(seed, which, idx.reshape(-1))
+    return out.reshape(len(pages), block_size, head_dim)
+
+
 def fill_pool_(pool: torch.Tensor, seed: int, which: str,
-               pages_per_chunk: int = 2048) -> torch.Tensor:
+               pages_per_chunk: int = 0) -> torch.Tensor:
     """Fill a bf16 pool [num_blocks, Hkv, P, D] in place, chunk by chunk."""
     nb, hkv, p, d = pool.shape
+    if pages_per_chunk <= 0:
+        pages_per_chunk = max(1, (1 << 26) // (hkv * p * d))
     for start in range(0, nb, pages_per_chunk):
         stop = min(nb, start + pages_per_chunk)
         ids = np.arange(start, stop, dtype=np.int64)
@@ -202,11 +215,14 @@ class Workload:
 
     # -- where the step's new tokens go -------------------------------------
     def decode_slot_mapping(self) -> np.ndarray:
-        """int64 [B]: pool slot (page*P + offset) of each decode token."""
+        """int64 [B]: pool slot (page*P + offset) of each decode token.
+
+        A sequence of length 0 appends nothing: its slot is -1 (skipped)."""
         pos = self.context_lens.astype(np.int64) - 1
         rows = np.arange(self.num_seqs)
-        page = self.block_tables[rows, pos // self.block_size].astype(np.int64)
-        return page * self.block_size + pos % self.block_size
+        page = self.block_tables[rows, np.maximum(pos, 0) // self.block_size].astype(np.int64)
+        slot = page * self.block_size + np.maximum(pos, 0) % self.block_size
+        return np.where(pos >= 0, slot, -1)
 
     def prefill_slot_mapping(self) -> np.ndarray:
         """int64 [T_p]: pool slots of the prefill chunk tokens, packed."""
