@@ -204,9 +204,9 @@ def cpu_baseline(w, target_s, gen_device):
 
 
 # ---------------------------------------------------------------------------
-def _workload(i):
+def _workload(i, num_seqs=None):
     import workloads as W
-    return W.config(i)
+    return W.config(i, num_seqs)
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -236,7 +236,7 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
-    w = _workload(args.workload)
+    w = _workload(args.workload, args.num_seqs)
     seqs = _sample_seqs(w, args.ref_sample_s)
     inp = _oracle_sample(w, seqs, "cpu")
     for _ in range(args.warmup):
@@ -285,7 +285,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = _workload(args.workload)
+    w = _workload(args.workload, args.num_seqs)
     peaks, peak_kind = _peaks()
 
     # --- inputs resident in HBM ---------------------------------------------------
@@ -423,6 +423,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition tokens (0 = library's automatic choice)")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="keep only the first N sequences (a smaller case, for profiling)")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
     ap.add_argument("--ref-sample-s", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -384,8 +384,30 @@ CONFIG_NAMES = {
 }
 
 
-def config(i: int) -> Workload:
-    """Configuration i (1..5) at full size; seed 31000 + i."""
+def config(i: int, num_seqs: Optional[int] = None) -> Workload:
+    """Configuration i (1..5) at full size; seed 31000 + i.
+
+    ``num_seqs`` keeps only the first sequences of the batch (same lengths,
+    same shapes, a pool sized for them): a smaller case of the same kernel,
+    e.g. for profiler captures."""
+    w = _config_full(i)
+    if num_seqs is None or num_seqs >= w.num_seqs:
+        return w
+    lens = w.context_lens[:num_seqs]
+    sharers = min(w.num_sharers, num_seqs)
+    if w.num_prefill:
+        return make_mixed(w.name + f"_first{num_seqs}", w.seed, lens, w.prefill_context_lens
+                          - w.prefill_chunk_lens, w.prefill_chunk_lens, w.num_q_heads,
+                          w.num_kv_heads, w.head_dim, w.block_size,
+                          max_blocks=w.max_blocks_per_seq)
+    return make_decode(w.name + f"_first{num_seqs}", w.seed, lens, w.num_q_heads,
+                       w.num_kv_heads, w.head_dim, w.block_size, kv_dtype=w.kv_dtype,
+                       max_blocks=w.max_blocks_per_seq,
+                       shared_tokens=w.shared_prefix_tokens if sharers > 1 else 0,
+                       num_sharers=sharers if sharers > 1 else 0)
+
+
+def _config_full(i: int) -> Workload:
     seed = 31000 + i
     rng = np.random.Generator(np.random.PCG64(seed))
     if i == 1:
