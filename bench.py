@@ -384,6 +384,7 @@ def run_gpu(args):
                              // w.block_size)) * 4 + B * 4)
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
+    launches_per_step = 3 + (1 if has_prefill else 0)   # append, plan, decode (+ prefill)
     part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,
                                                 w.k_scale, w.v_scale)
     splits = max_splits > 1

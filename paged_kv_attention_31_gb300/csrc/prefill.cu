@@ -54,7 +54,11 @@ constexpr int kOffV = kOffK + 2 * kKVStageBytes;
 constexpr int kOffP = kOffV + 2 * kKVStageBytes;
 constexpr int kOffBar = kOffP + kPBytes;     // barriers: q, k[2], v[2], s, o
 constexpr int kOffMisc = kOffBar + 8 * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+// The 128-byte-swizzled tiles need a 1024-aligned base.  Dynamic shared memory
+// starts at least 128-aligned, so at most 896 bytes of padding are needed;
+// with that slack two CTAs fit in one SM's 228 KB.
+constexpr int kMaxPad = 1024 - 128;
+constexpr int kSmemBytes = kOffMisc + 16 + kMaxPad;
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -156,7 +160,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   const int mt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
@@ -172,9 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > uint32_t(kMaxPad)) {  // cannot happen with a 128-aligned base; never index past the end
+    if (threadIdx.x == 0) record_error(p.err, kDevBadPage);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
