@@ -155,6 +155,39 @@ PKV_API pkv_status pkv_paged_attention(const void *q, const void *k_pool, const 
                                size_t workspace_bytes, void *out, void *stream);
 
 /*
+ * pkv_paged_attention_noalloc -- the same decode attention as
+ * pkv_paged_attention, for callers that cannot allocate device memory (the
+ * pages describe no counterpart; this is a library convenience).  Some
+ * callers receive only their input and output buffers -- a plugin run by a
+ * host engine that owns all device allocations and exposes no workspace, or
+ * a latency-critical step that must not call cudaMalloc -- so this entry
+ * point takes no workspace and allocates nothing.  Its scratch is a fixed
+ * device array inside the library of pkv_paged_attention_noalloc_max_scratch()
+ * bytes (64 MiB), held on every GPU that loads the library until the process
+ * exits.
+ *   Arguments as for pkv_paged_attention, minus workspace / workspace_bytes.
+ *   Returns PKV_ERR_WORKSPACE when these sizes need more scratch than the
+ *   fixed maximum (see pkv_paged_attention_workspace_size); nothing is
+ *   enqueued then.
+ *   The first call on a device resolves the array's device address (a host
+ *   call, once per device); make that first call before any stream capture.
+ *   Every call shares the one array and the scratch needs no initial
+ *   contents.  Calls whose work overlaps on the GPU (different streams
+ *   without ordering between them) race on the array and give wrong results.
+ */
+PKV_API pkv_status pkv_paged_attention_noalloc(const void *q, const void *k_pool,
+                                               const void *v_pool, const pkv_pool_desc *pool,
+                                               const int32_t *block_tables,
+                                               int32_t max_blocks_per_seq,
+                                               const int32_t *context_lens, int32_t num_seqs,
+                                               int32_t num_q_heads, int32_t max_context_len,
+                                               float scale, int32_t partition_tokens, void *out,
+                                               void *stream);
+
+/* Size in bytes of the fixed scratch array pkv_paged_attention_noalloc uses. */
+PKV_API size_t pkv_paged_attention_noalloc_max_scratch(void);
+
+/*
  * pkv_paged_prefill -- causal attention of prefill-chunk tokens over their
  * sequences' pages (§5.3 "分块上下文处理": chunked context).
  *

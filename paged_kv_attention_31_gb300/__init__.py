@@ -10,6 +10,7 @@ Functions mirror the C entry points:
     paged_attention_workspace_size  <- pkv_paged_attention_workspace_size
     paged_attention_plan            <- pkv_paged_attention_plan
     paged_attention                 <- pkv_paged_attention
+    paged_attention_noalloc         <- pkv_paged_attention_noalloc
     paged_prefill                   <- pkv_paged_prefill
     get_device_error                <- pkv_get_device_error
     status_string                   <- pkv_status_string
@@ -72,6 +73,11 @@ def lib():
             L.pkv_paged_attention.restype = i32
             L.pkv_paged_attention.argtypes = [vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, f32,
                                               i32, vp, sz, vp, vp]
+            L.pkv_paged_attention_noalloc.restype = i32
+            L.pkv_paged_attention_noalloc.argtypes = [vp, vp, vp, pd, vp, i32, vp, i32, i32, i32,
+                                                      f32, i32, vp, vp]
+            L.pkv_paged_attention_noalloc_max_scratch.restype = sz
+            L.pkv_paged_attention_noalloc_max_scratch.argtypes = []
             L.pkv_paged_prefill.restype = i32
             L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, i32,
                                             f32, vp, vp]
@@ -191,6 +197,30 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_l
                                      int(workspace.numel() * workspace.element_size()),
                                      _ptr(out), _stream(stream)),
            "pkv_paged_attention")
+    return out
+
+
+def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_context_len,
+                            scale, out=None, k_scale=1.0, v_scale=1.0, partition_tokens=0,
+                            stream=None) -> torch.Tensor:
+    """Decode attention without a workspace, for callers that cannot allocate
+    device scratch: the library's fixed device array is used instead (calls
+    must not overlap on the GPU; the first call on a device does a one-time
+    host set-up)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3:
+        raise TypeError("q must be bfloat16 [num_seqs, num_q_heads, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables / context_lens must be int32")
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().pkv_paged_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                             ctypes.byref(desc), _ptr(block_tables),
+                                             int(block_tables.shape[1]), _ptr(context_lens),
+                                             int(B), int(Hq), int(max_context_len), float(scale),
+                                             int(partition_tokens), _ptr(out), _stream(stream)),
+           "pkv_paged_attention_noalloc")
     return out
 
 
