@@ -36,8 +36,19 @@
 
 namespace pkv {
 
+// Per-warp bulk-copy ring depth and warps per CTA.  Two stages beat three or
+// four on GB300: the smaller ring lets three CTAs share an SM, and the extra
+// resident warps hide the tile compute's latency better than deeper
+// prefetch (measured on the Llama-2-13B and Llama-3-8B decode shapes).
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 2
+#endif
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+
 constexpr int kTT = 16;  // tokens per tile (divides every supported block size)
-constexpr int kNW = 4;   // warps per CTA
+constexpr int kNW = PKV_DECODE_WARPS;  // warps per CTA
 constexpr int kMaxBuckets = 1024;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -267,25 +278,27 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       pages[i] = pid;
     }
     // q of the G packed heads, pre-scaled into the log2 domain
-    float qf[G][E];
+    float2 q2[G][E / 2];  // (d, d+1) pairs for packed fp32 FMA
     {
       const __nv_bfloat16* qrow =
           static_cast<const __nv_bfloat16*>(p.q) + (size_t(s) * p.num_q_heads + size_t(h) * G) * D;
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int j = 0; j < C::NCH; ++j) load_q<EC>(qrow + g * D + (c + j * TPT) * EC, p.q_mult, &qf[g][j * EC]);
+        for (int j = 0; j < C::NCH; ++j)
+          load_q<EC>(qrow + g * D + (c + j * TPT) * EC, p.q_mult,
+                     reinterpret_cast<float*>(&q2[g][j * EC / 2]));
     }
     __syncthreads();  // pages[] visible
 
     const int ntile = (t1 - t0 + TT - 1) / TT;
     const int my_n = warp < ntile ? (ntile - warp + NW - 1) / NW : 0;
     float m_run = -INFINITY, l_run = 0.f;
-    float acc[G][DV];
+    float2 acc[G][DV / 2];  // (column, column+1) pairs
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < DV; ++e) acc[g][e] = 0.f;
+      for (int e = 0; e < DV / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
 
     // lane 0 issues the copies of this warp's j-th tile of the unit
     auto issue = [&](int j) {
@@ -320,18 +333,24 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       for (int ps = 0; ps < C::PASSES; ++ps) {
         const int t = ps * NT + tk;
         const uint8_t* row = kb + t * RB;
-        float part[G];
+        // packed fp32 FMAs: even and odd head_dim elements accumulate in the
+        // two halves of part2 and are added at the end
+        float2 part2[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = 0.f;
+        for (int g = 0; g < G; ++g) part2[g] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int jc = 0; jc < C::NCH; ++jc) {
-          float kf[EC];
-          load_cvt<FP8, EC>(row + (c + jc * TPT) * CB, kf);
+          float2 k2[EC / 2];
+          load_cvt<FP8, EC>(row + (c + jc * TPT) * CB, reinterpret_cast<float*>(k2));
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < EC; ++e) part[g] = fmaf(qf[g][jc * EC + e], kf[e], part[g]);
+            for (int e = 0; e < EC / 2; ++e)
+              part2[g] = __ffma2_rn(q2[g][jc * EC / 2 + e], k2[e], part2[g]);
         }
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = part2[g].x + part2[g].y;
         const float r = reduce_scatter<G, TPT>(part, c);
         if ((c & (TPT / G - 1)) == 0) sc[t * G + c / (TPT / G)] = t < ntok ? r : -INFINITY;
       }
@@ -378,13 +397,13 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       // ---- P V ------------------------------------------------------------------
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float a = al[g];
+        const float2 a = make_float2(al[g], al[g]);
 #pragma unroll
-        for (int e = 0; e < DV; ++e) acc[g][e] *= a;
+        for (int e = 0; e < DV / 2; ++e) acc[g][e] = __fmul2_rn(a, acc[g][e]);
       }
       auto pv = [&](int t) {
-        float vf[DV];
-        load_cvt<FP8, DV>(vb + t * RB + lane * DV * EB, vf);
+        float2 v2[DV / 2];
+        load_cvt<FP8, DV>(vb + t * RB + lane * DV * EB, reinterpret_cast<float*>(v2));
         float pg[G];
         if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -399,9 +418,11 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
           pg[0] = sc[t];
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) {
+          const float2 pp = make_float2(pg[g], pg[g]);
 #pragma unroll
-          for (int e = 0; e < DV; ++e) acc[g][e] = fmaf(pg[g], vf[e], acc[g][e]);
+          for (int e = 0; e < DV / 2; ++e) acc[g][e] = __ffma2_rn(pp, v2[e], acc[g][e]);
+        }
       };
       if (ntok == TT) {
 #pragma unroll
@@ -423,7 +444,8 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < DV; ++e) ca[(warp * G + g) * D + lane * DV + e] = acc[g][e];
+      for (int e = 0; e < DV / 2; ++e)
+        *reinterpret_cast<float2*>(&ca[(warp * G + g) * D + lane * DV + 2 * e]) = acc[g][e];
     if (threadIdx.x == 0) misc[1] = next;
     __syncthreads();
     const int next_unit = misc[1];
@@ -495,7 +517,7 @@ namespace {
 
 template <int D, int G, bool FP8>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  constexpr int ST = 3;
+  constexpr int ST = PKV_DECODE_STAGES;
   using C = DecodeCfg<D, G, FP8, ST>;
   auto kern = decode_kernel<D, G, FP8, ST>;
   const int max_pages = (p.partition + p.block_size - 1) / p.block_size + 1;
