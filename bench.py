@@ -315,9 +315,13 @@ def run_gpu(args):
         if ev is not None:
             ev[1].record(stream)
         if has_prefill:
+            if ev is not None:
+                ev[2].record(stream)
             pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp,
                               d["prefill_block_tables"], d["prefill_context_lens"], max_q,
                               w.scale, out=out_p)
+            if ev is not None:
+                ev[3].record(stream)
 
     args_dev = (d["q"], d["k_new"], d["v_new"], d["slots"], d["block_tables"], d["context_lens"])
     for _ in range(args.warmup):
@@ -327,7 +331,7 @@ def run_gpu(args):
         raise RuntimeError("device error during warm-up")
 
     # --- timed region: device-resident inputs -------------------------------------
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
            for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
@@ -345,7 +349,8 @@ def run_gpu(args):
         torch.distributed.barrier()
     clock_info = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_stop)
-    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    prefill_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs])) if has_prefill else None
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # --- end to end through the public API from pinned host memory ------------------
@@ -406,6 +411,16 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock_info,
     }
+    if has_prefill:
+        flops = w.prefill_flops()
+        tpeak = float(peaks["bf16_tflops"])
+        tflops = flops / (prefill_ms * 1e-3) / 1e12
+        line["prefill"] = {"kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
+                           "ms": prefill_ms, "flops_per_launch": flops,
+                           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpeak,
+                                        "unit": "TFLOP/s", "frac": tflops / tpeak,
+                                        "peak_kind": peak_kind,
+                                        "traffic": _ncu_traffic("prefill_kernel", w.name)}}
     if cpu_line is not None:
         line["cpu_baseline"] = cpu_line
     if rank == 0:

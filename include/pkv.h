@@ -203,6 +203,7 @@ PKV_API size_t pkv_paged_attention_noalloc_max_scratch(void);
  *   block_tables    device, int32 [num_seqs][max_blocks_per_seq]
  *   context_lens    device, int32 [num_seqs]
  *   max_q_len       host upper bound of C_s
+ *   scale           softmax scale, finite and > 0
  *   out             device, bf16 [num_q_tokens][num_q_heads][head_dim]
  * head_dim must be 128; the group size num_q_heads/num_kv_heads must divide
  * 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
@@ -222,6 +223,10 @@ PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
  * since the last call).  Returns PKV_ERR_CUDA if the synchronisation fails.
  */
 PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
+
+/* Text of the last CUDA error a call of this library met on the calling
+ * thread (explains PKV_ERR_CUDA; "no error" if none).  Never NULL. */
+PKV_API const char *pkv_last_cuda_error(void);
 
 /* Static string for a status code (never NULL). */
 PKV_API const char *pkv_status_string(int32_t status);

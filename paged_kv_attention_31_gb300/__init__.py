@@ -40,7 +40,10 @@ _lib = None
 class PkvError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        msg = f"{what}: {status_string(status)} (status {status})"
+        if status == 4:  # PKV_ERR_CUDA
+            msg += f": {lib().pkv_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 class PoolDesc(ctypes.Structure):
@@ -83,6 +86,8 @@ def lib():
                                             f32, vp, vp]
             L.pkv_get_device_error.restype = i32
             L.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
+            L.pkv_last_cuda_error.restype = ctypes.c_char_p
+            L.pkv_last_cuda_error.argtypes = []
             L.pkv_status_string.restype = ctypes.c_char_p
             L.pkv_status_string.argtypes = [i32]
             L.pkv_version.restype = i32

@@ -241,12 +241,16 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
   int* const misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
   int* const pages = reinterpret_cast<int*>(smem + C::OFF_PG);
 
+  volatile int* const abort_flag = misc + 2;  // raised by a timed-out wait
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < ST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
-  if (threadIdx.x == 0) misc[0] = atomicAdd(p.counters + 1, 1);
+  if (threadIdx.x == 0) {
+    misc[0] = atomicAdd(p.counters + 1, 1);
+    misc[2] = 0;
+  }
   __syncthreads();
 
   const int Hkv = p.num_kv_heads, P = p.block_size;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       const uint32_t parity = ((jt + j) / ST) & 1;
       const int ts = t0 + (warp + j * NW) * TT;
       const int ntok = pages[ts / P - pg0] < 0 ? 0 : min(TT, t1 - ts);
-      mbar_wait_bounded(&bars[stage], parity, p.err);
+      mbar_wait_bounded(&bars[stage], parity, p.err, abort_flag);
       const uint8_t* kb = kbuf + stage * TB;
       const uint8_t* vb = vbuf + stage * TB;
 

@@ -57,8 +57,11 @@ pkv_status check_pool(const pkv_pool_desc* pool) {
   return PKV_OK;
 }
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 pkv_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return PKV_OK;
+  g_last_cuda_error = e;
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return PKV_ERR_CUDA;
 }
@@ -95,6 +98,8 @@ pkv_status validate_partition(int32_t partition, int block_size) {
 extern "C" {
 
 int32_t pkv_version(void) { return 100; }
+
+const char* pkv_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 const char* pkv_status_string(int32_t s) {
   switch (s) {
@@ -260,7 +265,7 @@ pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const v
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / pool->num_kv_heads;
   if (G > 128 || 128 % G != 0) return PKV_ERR_UNSUPPORTED;
-  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale) || !(scale > 0.f)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0 || num_q_tokens == 0 || max_q_len == 0) return PKV_OK;
   if (!q || !cu_seqlens_q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
     return PKV_ERR_INVALID_ARG;

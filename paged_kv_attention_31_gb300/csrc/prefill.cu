@@ -5,29 +5,36 @@
 // is processed as chunks interleaved with decode steps; each chunk's queries
 // attend causally to everything before them in the sequence, whose K/V sit
 // in pages (§4.2, §6.2).  §6.1 (Flash Attention实现): 64-128-token key tiles,
-// running max / sum, partial results kept on chip.
+// double buffering, running max / sum, partial results kept on chip.
 //
-// One CTA computes one 128-row query tile of one (sequence, kv head).  The
-// 128 rows pack TQ = 128/G chunk tokens x the G q heads that share the kv
-// head (row r = token (r / G), head g = r % G), so every K/V page is read
-// once per kv head and the tile is a dense M = 128 contraction.
-//
-// Per key block of NK = 64 keys (NK / block_size pages):
-//   TMA     each page (block_size rows x 128 B, one box per d-half) lands in a
-//           128-byte-swizzled shared-memory tile; page ids come from the block
-//           table; pages past the sequence use an out-of-range coordinate, so
-//           TMA fills zeros.
-//   S       tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), M=128 N=64 K=128,
-//           Q and K both K-major in shared memory, S accumulates in TMEM.
-//   softmax each of the 128 threads owns one row (TMEM lane): tcgen05.ld the
-//           64 scores, causal mask, running max kept with a lag of up to 2^8
-//           (the O accumulator is rescaled only when the max grows by more
-//           than that; the normalisation at the end uses the same max, so the
-//           result is exact), P = 2^(s - m) rounded to bf16 into shared memory.
-//   PV      tcgen05.mma M=128 N=128 K=64, P K-major, V MN-major (d contiguous),
-//           O accumulates in TMEM.
-// K/V use a two-stage ring with separate K and V barriers so the next K block
-// loads while the current block's softmax and PV run.
+// A query tile is 128 rows: TQ = 128/G chunk tokens x the G q heads that
+// share one kv head (row r = token r / G, head r % G), so every K/V page is
+// read once per kv head and the tile is a dense M = 128 contraction.  One CTA
+// (one per SM) takes two consecutive tiles of one (sequence, kv head) and
+// specialises its warps:
+//   warps 9, 10 loaders: TMA of Q and the K pages (warp 9) and of the V
+//               pages (warp 10) into 3-stage rings of 64-key blocks shared by
+//               both tiles; page ids from the block table, read a few
+//               blocks ahead; pages past the sequence use an out-of-range
+//               coordinate so TMA fills zeros.  Keeping loads out of the MMA
+//               warp keeps their latencies off the tensor core's issue path.
+//   warp 8      every tcgen05.mma (one elected lane):
+//                 S_t = Q_t K_j^T  (M=128, N=64, K=128 -> TMEM, fp32)
+//                 O_t += P_t V_j   (M=128, N=128, K=64 -> TMEM, fp32)
+//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: one thread
+//   warps 4-7   per row (TMEM lane): tcgen05.ld of S, causal mask, running
+//               max kept with a lag of up to 2^8 (O is rescaled in TMEM only
+//               when the max grows by more; the final normalisation uses the
+//               same max, so the result is exact), P = 2^(s - m) rounded to
+//               bf16 into 128-byte-swizzled shared memory.
+// Hand-offs are mbarriers only: tcgen05.commit signals "S ready", "O
+// updated" and "K / V stage free"; the softmax warps signal "P ready".  S is
+// double-buffered per tile in TMEM and issued two key blocks ahead, so the
+// next scores are ready when a softmax warpgroup finishes a block; while one
+// tile's softmax runs, the tensor core works on the other tile.  P is
+// double-buffered per tile too, so a warpgroup writes block j + 1's P while
+// the PV of block j still runs; only a rescale of O waits for the latest PV.
+// K and V have separate 3-stage rings (K is needed two blocks before V).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,25 +47,34 @@ namespace {
 constexpr int kD = 128;          // head_dim
 constexpr int kM = 128;          // query rows per tile
 constexpr int kNK = 64;          // keys per block
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;  // S: cols [0, 64), O: cols [128, 256)
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr int kTiles = 2;        // query tiles per CTA
+constexpr int kStages = 3;       // K/V ring depth (key blocks)
+constexpr int kSoftmaxThreads = 128 * kTiles;
+constexpr int kMmaWarp = kSoftmaxThreads / 32;   // warp 8: issues every tcgen05.mma
+constexpr int kKLoadWarp = kMmaWarp + 1;         // warp 9: TMA of Q and of the K ring
+constexpr int kVLoadWarp = kMmaWarp + 2;         // warp 10: TMA of the V ring
+constexpr int kThreads = kSoftmaxThreads + 3 * 32;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S of tile t, buffer b at 64 (2 t + b); O of tile t at 256 + 128 t
+constexpr uint32_t kColS = 0, kColO = 256;
 
 // shared memory layout (offsets from a 1024-aligned base)
-constexpr int kQBytes = 2 * kM * 128;        // 32 KB: two d-halves of [128 rows][128 B]
+constexpr int kQBytes = 2 * kM * 128;        // 32 KB per tile: two d-halves of [128 rows][128 B]
 constexpr int kKVStageBytes = 2 * kNK * 128; // 16 KB: two d-halves of [64 keys][128 B]
-constexpr int kPBytes = kM * 128;            // 16 KB: [128 rows][64 keys bf16]
+constexpr int kPBytes = kM * 128;            // 16 KB per tile and buffer: [128 rows][64 keys bf16]
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + 2 * kKVStageBytes;
-constexpr int kOffP = kOffV + 2 * kKVStageBytes;
-constexpr int kOffBar = kOffP + kPBytes;     // barriers: q, k[2], v[2], s, o
-constexpr int kOffMisc = kOffBar + 8 * 8;
-// The 128-byte-swizzled tiles need a 1024-aligned base.  Dynamic shared memory
-// starts at least 128-aligned, so at most 896 bytes of padding are needed;
-// with that slack two CTAs fit in one SM's 228 KB.
+constexpr int kOffK = kOffQ + kTiles * kQBytes;
+constexpr int kOffV = kOffK + kStages * kKVStageBytes;
+constexpr int kOffP = kOffV + kStages * kKVStageBytes;
+constexpr int kOffBar = kOffP + 2 * kTiles * kPBytes;  // P double-buffered per tile
+// barriers: q, k[3], v[3], kfree[3], vfree[3], s[2][2], p[2][2], o[2][2]
+constexpr int kNumBars = 1 + 4 * kStages + 6 * kTiles;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+// The 128-byte-swizzled tiles need a 1024-aligned base; dynamic shared memory
+// starts at least 128-aligned, so at most 896 bytes of padding are needed.
 constexpr int kMaxPad = 1024 - 128;
 constexpr int kSmemBytes = kOffMisc + 16 + kMaxPad;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -160,15 +176,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// The register file is handed out per group of four warps, so the 9-warp
+// CTA is budgeted as 12 warps: at most 168 registers per thread.
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  const int mt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  // heavier (later, longer-context) tile pairs are launched first
+  const int pair = int(gridDim.x) - 1 - int(blockIdx.x);
+  const int h = blockIdx.y, s = blockIdx.z;
   const int G = p.num_q_heads / p.num_kv_heads;
   const int TQ = kM / G;
   const int q0 = __ldg(p.cu_seqlens_q + s);
   const int C = __ldg(p.cu_seqlens_q + s + 1) - q0;
-  if (C <= 0 || mt * TQ >= C) return;
+  const int tokA = pair * kTiles * TQ;            // first chunk token of tile 0
+  if (C <= 0 || tokA >= C) return;
   const int L = __ldg(p.context_lens + s);
   const int P = p.block_size;
   if (L < C || L > p.max_blocks * P) {
@@ -188,30 +209,46 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* sV = smem + kOffV;
   uint8_t* sP = smem + kOffP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* bar_q = bar + 0;
-  uint64_t* bar_k = bar + 1;  // [2]
-  uint64_t* bar_v = bar + 3;  // [2]
-  uint64_t* bar_s = bar + 5;
-  uint64_t* bar_o = bar + 6;
+  uint64_t* bar_q = bar;
+  uint64_t* bar_k = bar + 1;                      // [kStages] K block landed
+  uint64_t* bar_v = bar_k + kStages;              // [kStages] V block landed
+  uint64_t* bar_kfree = bar_v + kStages;          // [kStages] S MMAs done with the K stage
+  uint64_t* bar_vfree = bar_kfree + kStages;      // [kStages] PV MMAs done with the V stage
+  // per tile t and buffer b = block & 1 (one barrier per buffer, so a side
+  // that runs a block ahead never aliases a phase):
+  uint64_t* bar_s = bar_vfree + kStages;          // [kTiles][2] S_t buffer ready
+  uint64_t* bar_p = bar_s + 2 * kTiles;           // [kTiles][2] P_t buffer written (4 warps)
+  uint64_t* bar_o = bar_p + 2 * kTiles;           // [kTiles][2] PV from that P buffer done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int tok0 = mt * TQ;                      // first chunk token of the tile
-  const int ntok = min(TQ, C - tok0);
-  const int minpos = L - C + tok0;               // position of the tile's first token
-  const int maxpos = L - C + tok0 + ntok - 1;    // position of its last token
-  const int nblk = maxpos / kNK + 1;             // key blocks 0 .. nblk-1
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // per-tile extent: valid tokens, first position, key blocks to visit
+  static_assert(kTiles == 2, "two query tiles per CTA");
+  const int ntok0 = max(0, min(TQ, C - tokA));
+  const int ntok1 = max(0, min(TQ, C - (tokA + TQ)));
+  const int nb0 = ntok0 > 0 ? (L - C + tokA + ntok0 - 1) / kNK + 1 : 0;
+  const int nb1 = ntok1 > 0 ? (L - C + tokA + TQ + ntok1 - 1) / kNK + 1 : 0;
+  const int nblk = max(nb0, nb1);                 // key blocks loaded for the CTA
   const int npages = (L + P - 1) / P;
   const int pages_per_blk = kNK / P;
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(&bar_k[0], 1);
-    mbar_init(&bar_k[1], 1);
-    mbar_init(&bar_v[0], 1);
-    mbar_init(&bar_v[1], 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar_k[i], 1);
+      mbar_init(&bar_v[i], 1);
+      mbar_init(&bar_kfree[i], 1);
+      mbar_init(&bar_vfree[i], 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bar_s[2 * t + b], 1);
+        mbar_init(&bar_p[2 * t + b], 4);
+        mbar_init(&bar_o[2 * t + b], 1);
+      }
+    }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -219,11 +256,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = uint32_t(warp * 32) << 16;
 
-  // page id of logical page j, or an out-of-range id (TMA fills zeros)
+  // ============================ loaders and MMA issuer ============================
   auto page_of = [&](int j) -> int {
-    if (j >= npages) return p.num_blocks;
+    if (j >= npages) return p.num_blocks;  // past the sequence: TMA zero fill
     int pid = __ldg(p.block_tables + size_t(s) * p.max_blocks + j);
     if (pid < 0 || pid >= p.num_blocks) {
       record_error(p.err, kDevBadPage);
@@ -231,181 +267,270 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     return pid;
   };
-  auto load_kv = [&](const CUtensorMap* map, uint8_t* base, uint64_t* b, int blk) {
-    mbar_arrive_expect_tx(b, kKVStageBytes);
-    for (int i = 0; i < pages_per_blk; ++i) {
-      const int pid = page_of(blk * pages_per_blk + i);
+  // loader warps: lane i holds the id of page i of key block `blk`
+  auto fetch_ids = [&](int blk) -> int {
+    return (lane < pages_per_blk && blk < nblk) ? page_of(blk * pages_per_blk + lane) : 0;
+  };
+  // TMA of one key block's pages into its ring stage (whole loader warp)
+  auto load_blk = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* bars, int blk, int ids) {
+    const int st = blk % kStages;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], kKVStageBytes);
 #pragma unroll
-      for (int dh = 0; dh < 2; ++dh)
-        tma_load_4d(base + dh * (kNK * 128) + i * P * 128, map, dh * 64, 0, h, pid, b);
+    for (int i = 0; i < kNK / 16; ++i) {  // at most 4 pages per block (block_size >= 16)
+      const int pid = __shfl_sync(0xffffffffu, ids, i);
+      if (lane == 0 && i < pages_per_blk) {
+#pragma unroll
+        for (int dh = 0; dh < 2; ++dh)
+          tma_load_4d(ring + st * kKVStageBytes + dh * (kNK * 128) + i * P * 128, map, dh * 64,
+                      0, h, pid, &bars[st]);
+      }
+    }
+  };
+  // a loader streams blocks 0 .. nblk-1 into its ring; block b reuses the
+  // stage of block b - kStages once `freed` says the MMAs reading it are done
+  auto run_loader = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* freed) {
+    constexpr int kLead = 4;  // page ids are read kLead blocks ahead
+    int ids[kLead];
+#pragma unroll
+    for (int k = 0; k < kLead; ++k) ids[k] = fetch_ids(k);
+    for (int b = 0; b < nblk; ++b) {
+      if (b >= kStages)
+        mbar_wait_bounded(&freed[b % kStages], uint32_t((b - kStages) / kStages) & 1, p.err,
+                          abort_flag);
+      load_blk(map, ring, full, b, ids[0]);
+#pragma unroll
+      for (int k = 0; k + 1 < kLead; ++k) ids[k] = ids[k + 1];
+      ids[kLead - 1] = fetch_ids(b + kLead);
     }
   };
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_q, kQBytes);
+  if (warp == kKLoadWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, kTiles * kQBytes);
+      for (int t = 0; t < kTiles; ++t)
 #pragma unroll
-    for (int dh = 0; dh < 2; ++dh) tma_load_4d(sQ + dh * (kM * 128), &tm_q, dh * 64, 0, h, q0 + tok0, bar_q);
-    load_kv(&tm_k, sK, &bar_k[0], 0);
-    load_kv(&tm_v, sV, &bar_v[0], 0);
-    if (nblk > 1) {
-      load_kv(&tm_k, sK + kKVStageBytes, &bar_k[1], 1);
-      load_kv(&tm_v, sV + kKVStageBytes, &bar_v[1], 1);
+        for (int dh = 0; dh < 2; ++dh)
+          tma_load_4d(sQ + t * kQBytes + dh * (kM * 128), &tm_q, dh * 64, 0, h,
+                      q0 + tokA + t * TQ, bar_q);
     }
-  }
-
-  // this thread's query row
-  const int row = tid;
-  const int tok = tok0 + row / G;
-  const bool row_valid = (row / G) < ntok;
-  const int pos = row_valid ? L - C + tok : -1;  // keys 0 .. pos are visible
-  float m_used = -INFINITY, l_sum = 0.f;
-  const float qm = p.q_mult;
-  constexpr uint32_t kIdescS = idesc_bf16(kM, kNK, false);
-  constexpr uint32_t kIdescO = idesc_bf16(kM, kD, true);
-
-  for (int j = 0; j < nblk; ++j) {
-    const int st = j & 1;
-    const uint32_t use_par = uint32_t(j >> 1) & 1;
-    // ---- S = Q K^T ---------------------------------------------------------------
-    if (tid == 0) {
-      if (j == 0) mbar_wait_bounded(bar_q, 0, p.err);
-      mbar_wait_bounded(&bar_k[st], use_par, p.err);
-      tc_fence_after();
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK + st * kKVStageBytes);
+    run_loader(&tm_k, sK, bar_k, bar_kfree);
+  } else if (warp == kVLoadWarp) {
+    run_loader(&tm_v, sV, bar_v, bar_vfree);
+  } else if (warp == kMmaWarp) {
+    constexpr uint32_t kIdescS = idesc_bf16(kM, kNK, false);
+    constexpr uint32_t kIdescO = idesc_bf16(kM, kD, true);
+    auto issue_s = [&](int t, int blk) {  // lane 0: S_t of block blk -> buffer blk & 1
+      const uint32_t qa = smem_u32(sQ + t * kQBytes);
+      const uint32_t ka = smem_u32(sK + (blk % kStages) * kKVStageBytes);
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
         const int dh = ks >> 2, w = ks & 3;
         const uint64_t ad = sw128_desc(qa + dh * (kM * 128) + w * 32, 16, 1024);
         const uint64_t bd = sw128_desc(ka + dh * (kNK * 128) + w * 32, 16, 1024);
-        mma_bf16(tmem + kColS, ad, bd, kIdescS, ks > 0);
+        mma_bf16(tmem + kColS + (2 * t + (blk & 1)) * kNK, ad, bd, kIdescS, ks > 0);
       }
-      mma_commit(bar_s);
-      // K of block j-1 was consumed by S_{j-1} (complete): refill its stage
-      if (j >= 1 && j + 1 < nblk) load_kv(&tm_k, sK + ((j + 1) & 1) * kKVStageBytes, &bar_k[(j + 1) & 1], j + 1);
-    }
-    mbar_wait_bounded(bar_s, uint32_t(j) & 1, p.err);
-    tc_fence_after();
-
-    // ---- scores of this row --------------------------------------------------------
-    float sv[kNK];
-    tmem_ld32(tmem + lane_base + kColS, sv);
-    tmem_ld32(tmem + lane_base + kColS + 32, sv + 32);
-    const int kbase = j * kNK;
-    float mx = -INFINITY;
-    if (kbase + kNK - 1 <= minpos) {       // block fully visible to every valid row
-#pragma unroll
-      for (int c = 0; c < kNK; ++c) {
-        sv[c] = row_valid ? sv[c] * qm : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < kNK; ++c) {
-        sv[c] = (kbase + c <= pos) ? sv[c] * qm : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
-      }
-    }
-    // lagged running max: move it only when the block max exceeds it by > 8
-    float alpha = 1.f;
-    if (mx > m_used + 8.f || (m_used == -INFINITY && mx != -INFINITY)) {
-      alpha = fast_exp2(m_used - mx);    // 0 when m_used = -inf
-      m_used = mx;
-      l_sum *= alpha;
-    }
-
-    // PV_{j-1} must be done before P is overwritten and O is rescaled
-    if (j > 0) {
-      mbar_wait_bounded(bar_o, uint32_t(j - 1) & 1, p.err);
-      tc_fence_after();
-      if (tid == 0 && j + 1 < nblk)
-        load_kv(&tm_v, sV + ((j + 1) & 1) * kKVStageBytes, &bar_v[(j + 1) & 1], j + 1);
-      // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs
-      // it (rows that do not have alpha == 1)
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int cc = 0; cc < kD; cc += 32) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + kColO + cc, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + lane_base + kColO + cc, o);
-        }
-      }
-    }
-
-    // ---- P = 2^(s - m) in bf16, swizzled K-major rows of 128 B ----------------------
-    float psum = 0.f;
-    uint8_t* prow = sP + row * 128;
-#pragma unroll
-    for (int c8 = 0; c8 < kNK / 8; ++c8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = m_used == -INFINITY ? 0.f : fast_exp2(sv[c8 * 8 + 2 * i] - m_used);
-        const float b = m_used == -INFINITY ? 0.f : fast_exp2(sv[c8 * 8 + 2 * i + 1] - m_used);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(a, b);
-        const float2 back = __bfloat1622float2(pb);
-        psum += back.x + back.y;
-        w[i] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    l_sum += psum;
-
-    // V rows past the sequence end may hold anything (never-written slots):
-    // zero them so 0 * V stays 0 in the PV product
-    if (kbase + kNK > L) {
-      mbar_wait_bounded(&bar_v[st], use_par, p.err);
-      const int first = max(0, L - kbase);
-      for (int i = tid; i < (kNK - first) * 2 * 8; i += kThreads) {
-        const int r = first + (i >> 4), rest = i & 15;
-        const int dh = rest >> 3, chunk = rest & 7;
-        *reinterpret_cast<uint4*>(sV + st * kKVStageBytes + dh * (kNK * 128) + r * 128 + chunk * 16) =
-            make_uint4(0, 0, 0, 0);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- O += P V ---------------------------------------------------------------------
-    if (tid == 0) {
-      mbar_wait_bounded(&bar_v[st], use_par, p.err);
-      tc_fence_after();
-      const uint32_t pa = smem_u32(sP), va = smem_u32(sV + st * kKVStageBytes);
+      mma_commit(&bar_s[2 * t + (blk & 1)]);
+    };
+    auto issue_pv = [&](int t, int blk) {  // lane 0: O_t += P_t(buffer blk & 1) V_blk
+      const uint32_t pa = smem_u32(sP + (2 * t + (blk & 1)) * kPBytes);
+      const uint32_t va = smem_u32(sV + (blk % kStages) * kKVStageBytes);
 #pragma unroll
       for (int ks = 0; ks < kNK / 16; ++ks) {
         const uint64_t ad = sw128_desc(pa + ks * 32, 16, 1024);
         const uint64_t bd = sw128_desc(va + ks * 2048, kNK * 128, 1024);
-        mma_bf16(tmem + kColO, ad, bd, kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
+        mma_bf16(tmem + kColO + t * kD, ad, bd, kIdescO, (blk > 0 || ks > 0) ? 1u : 0u);
       }
-      mma_commit(bar_o);
-    }
-  }
+      mma_commit(&bar_o[2 * t + (blk & 1)]);
+    };
+    auto wait_k = [&](int b) {
+      mbar_wait_bounded(&bar_k[b % kStages], uint32_t(b / kStages) & 1, p.err, abort_flag);
+    };
 
-  // ---- epilogue: O / l -> bf16 -------------------------------------------------------
-  mbar_wait_bounded(bar_o, uint32_t(nblk - 1) & 1, p.err);
-  tc_fence_after();
-  const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                       (size_t(q0 + tok) * p.num_q_heads + size_t(h) * G + (row % G)) * kD;
+    // S of blocks 0 and 1 (S runs two blocks ahead of the softmax)
+    mbar_wait_bounded(bar_q, 0, p.err, abort_flag);
+    for (int b = 0; b < 2 && b < nblk; ++b) {
+      wait_k(b);
+      if (lane == 0) {
+        tc_fence_after();
+        if (b < nb0) issue_s(0, b);
+        if (b < nb1) issue_s(1, b);
+        mma_commit(&bar_kfree[b % kStages]);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; j < nblk; ++j) {
+      const int st = j % kStages;
+      // V_j landed; rows past the sequence end may hold never-written slots:
+      // zero them so that 0 * V stays 0 in the PV product
+      mbar_wait_bounded(&bar_v[st], uint32_t(j / kStages) & 1, p.err, abort_flag);
+      if (j * kNK + kNK > L) {
+        const int first = max(0, L - j * kNK);
+        for (int i = lane; i < (kNK - first) * 16; i += 32) {
+          const int r = first + (i >> 4), dh = (i >> 3) & 1, chunk = i & 7;
+          *reinterpret_cast<uint4*>(sV + st * kKVStageBytes + dh * (kNK * 128) + r * 128 +
+                                    chunk * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      // O_t += P_t V_j once the softmax warps have written P_t; P_t also says
+      // S_t of block j has been read, so that buffer takes block j + 2
 #pragma unroll
-  for (int cc = 0; cc < kD; cc += 32) {
-    float o[32];
-    tmem_ld32(tmem + lane_base + kColO + cc, o);
-    if (row_valid) {
+      for (int t = 0; t < kTiles; ++t) {
+        const int nbt = t == 0 ? nb0 : nb1;
+        if (j >= nbt) continue;
+        mbar_wait_bounded(&bar_p[2 * t + (j & 1)], uint32_t(j >> 1) & 1, p.err, abort_flag);
+        if (lane == 0) {
+          tc_fence_after();
+          issue_pv(t, j);
+        }
+        __syncwarp();
+        if (j + 2 < nbt) {
+          wait_k(j + 2);
+          if (lane == 0) issue_s(t, j + 2);
+          __syncwarp();
+        }
+      }
+      // stage release: V_j after both tiles' PV, K_{j+2} after both tiles' S
+      if (lane == 0) {
+        mma_commit(&bar_vfree[st]);
+        if (j + 2 < nblk) mma_commit(&bar_kfree[(j + 2) % kStages]);
+      }
+      __syncwarp();
+    }
+  } else if (warp < kMmaWarp) {
+    // ================================ softmax ====================================
+    const int t = warp >> 2;                        // tile of this warpgroup
+    const int row = tid & 127;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t colO = kColO + t * kD;
+    const int tok = tokA + t * TQ + row / G;
+    const bool row_valid = (row / G) < (t == 0 ? ntok0 : ntok1);
+    const int pos = row_valid ? L - C + tok : -1;  // keys 0 .. pos are visible
+    const int minpos = L - C + tokA + t * TQ;      // first token of the tile
+    const float qm = p.q_mult;                     // scale * log2(e) > 0
+    uint8_t* const prow0 = sP + 2 * t * kPBytes + row * 128;  // buffer 0; buffer 1 follows
+    float m_used = -INFINITY, l_sum = 0.f;
+    const int nb = t == 0 ? nb0 : nb1;
+
+    for (int j = 0; j < nb; ++j) {
+      // S_t of block j sits in buffer j & 1 (the producer runs two blocks ahead)
+      mbar_wait_bounded(&bar_s[2 * t + (j & 1)], uint32_t(j >> 1) & 1, p.err, abort_flag);
+      tc_fence_after();
+      const uint32_t colS = kColS + (2 * t + (j & 1)) * kNK;
+      float sv[kNK];
+      tmem_ld32(tmem + lane_base + colS, sv);
+      tmem_ld32(tmem + lane_base + colS + 32, sv + 32);
+      const int kbase = j * kNK;
+      if (!row_valid) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        uint4 u;
-        __nv_bfloat162 b0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
-        __nv_bfloat162 b1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
-        __nv_bfloat162 b3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
-        u.x = *reinterpret_cast<uint32_t*>(&b0);
-        u.y = *reinterpret_cast<uint32_t*>(&b1);
-        u.z = *reinterpret_cast<uint32_t*>(&b2);
-        u.w = *reinterpret_cast<uint32_t*>(&b3);
-        *reinterpret_cast<uint4*>(dst + cc + i) = u;
+        for (int c = 0; c < kNK; ++c) sv[c] = -INFINITY;
+      } else if (kbase + kNK - 1 > minpos) {  // diagonal block: causal mask
+#pragma unroll
+        for (int c = 0; c < kNK; ++c) sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
+      }
+      // max as an 8-way tree (short dependency chains)
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+#pragma unroll
+      for (int c = 8; c < kNK; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= qm;  // raw-score max -> log2 domain (qm > 0)
+      // lagged running max: move it only when the block max exceeds it by > 8
+      float alpha = 1.f;
+      if (mx > m_used + 8.f) {
+        alpha = fast_exp2(m_used - mx);  // 0 when m_used = -inf
+        m_used = mx;
+        l_sum *= alpha;
+      }
+      // P = 2^(s * qm - m) -> bf16 pairs; the row sum stays in fp32
+      uint32_t pw[kNK / 2];
+      float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+      if (m_used != -INFINITY) {
+        const float negm = -m_used;
+#pragma unroll
+        for (int c = 0; c < kNK; c += 2) {
+          const float2 e2 = make_float2(fast_exp2(fmaf(sv[c], qm, negm)),
+                                        fast_exp2(fmaf(sv[c + 1], qm, negm)));
+          acc2[(c >> 1) & 3] = __fadd2_rn(acc2[(c >> 1) & 3], e2);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
+          pw[c / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kNK / 2; ++c) pw[c] = 0u;
+      }
+      const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      l_sum += a.x + a.y;
+
+      // P buffer j & 1 was last read by PV of block j - 2: wait for it.  A
+      // rescale of O needs every PV so far (block j - 1) to be done; it is rare
+      // (the running max moves by > 2^8 only early in a row).
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (rescale) {
+        mbar_wait_bounded(&bar_o[2 * t + ((j - 1) & 1)], uint32_t((j - 1) >> 1) & 1, p.err,
+                          abort_flag);
+      } else if (j > 1) {
+        mbar_wait_bounded(&bar_o[2 * t + (j & 1)], uint32_t((j - 2) >> 1) & 1, p.err, abort_flag);
+      }
+      if (j > 0) {
+        tc_fence_after();
+        // tcgen05.ld/st are warp-collective: the whole warp rescales (rows
+        // that do not need it multiply by 1)
+        if (rescale) {
+#pragma unroll 1
+          for (int cc = 0; cc < kD; cc += 32) {  // 32 columns at a time: bounded registers
+            float o[32];
+            tmem_ld32(tmem + lane_base + colO + cc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + lane_base + colO + cc, o);
+          }
+        }
+      }
+      uint8_t* const prow = prow0 + (j & 1) * kPBytes;
+#pragma unroll
+      for (int c8 = 0; c8 < kNK / 8; ++c8)
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
+            make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[2 * t + (j & 1)]);
+    }
+
+    // ---- epilogue: O / l -> bf16 ----------------------------------------------------
+    if (nb > 0) {
+      // the last PV's commit also covers every earlier MMA of the producer
+      mbar_wait_bounded(&bar_o[2 * t + ((nb - 1) & 1)], uint32_t((nb - 1) >> 1) & 1, p.err,
+                        abort_flag);
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                           (size_t(q0 + tok) * p.num_q_heads + size_t(h) * G + (row % G)) * kD;
+#pragma unroll 1
+      for (int cc = 0; cc < kD; cc += 32) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + colO + cc, o);
+        if (row_valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 u;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
+            u.x = *reinterpret_cast<uint32_t*>(&b0);
+            u.y = *reinterpret_cast<uint32_t*>(&b1);
+            u.z = *reinterpret_cast<uint32_t*>(&b2);
+            u.w = *reinterpret_cast<uint32_t*>(&b3);
+            *reinterpret_cast<uint4*>(dst + cc + i) = u;
+          }
+        }
       }
     }
   }
@@ -476,7 +601,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(p.tiles_per_seq, p.num_kv_heads, p.num_seqs);
+  // one CTA per pair of 128-row query tiles
+  dim3 grid((p.tiles_per_seq + kTiles - 1) / kTiles, p.num_kv_heads, p.num_seqs);
   if (grid.z > 65535) return cudaErrorInvalidValue;
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -279,6 +279,16 @@ class Workload:
             toks -= (self.num_sharers - 1) * self.shared_prefix_tokens
         return toks * per_tok
 
+    def prefill_flops(self) -> int:
+        """Causal-exact flops of the prefill attention (QK^T and PV, 2 flops
+        per multiply-add): chunk token i of sequence s sees L - C + i + 1 keys."""
+        total = 0
+        for s in range(self.num_prefill):
+            L, C = int(self.prefill_context_lens[s]), int(self.prefill_chunk_lens[s])
+            keys = C * (L - C) + C * (C + 1) // 2
+            total += keys * self.num_q_heads * 4 * self.head_dim
+        return total
+
     def decode_step_bytes(self, unique: bool = True) -> int:
         """Algorithmic bytes of one decode step (append + attention)."""
         B, Hq, Hkv, D = self.num_seqs, self.num_q_heads, self.num_kv_heads, self.head_dim
