@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "decode_mma.cu", "prefill.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -521,6 +521,10 @@ namespace {
 
 template <int D, int G, bool FP8>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  // FP8 KV with 4-8 packed q heads: the per-token work (G multiply-adds per
+  // byte for QK and again for PV) outruns the CUDA cores; it runs on
+  // warp-level tensor-core MMAs instead (decode_mma.cu)
+  if constexpr (FP8 && D == 128 && (G == 4 || G == 8)) return launch_decode_mma(p, num_sms, stream);
   constexpr int ST = PKV_DECODE_STAGES;
   using C = DecodeCfg<D, G, FP8, ST>;
   auto kern = decode_kernel<D, G, FP8, ST>;
@@ -565,6 +569,18 @@ cudaError_t launch_g(const DecodeParams& p, int num_sms, cudaStream_t stream) {
 }
 
 }  // namespace
+
+void launch_decode_plan(const DecodeParams& p, cudaStream_t stream) {
+  decode_plan_kernel<<<1, 512, 0, stream>>>(p);
+}
+
+void launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
+  const int warps = p.num_seqs * p.num_q_heads;
+  if (p.head_dim == 128)
+    decode_merge_kernel<128><<<(warps + 7) / 8, 256, 0, stream>>>(p);
+  else
+    decode_merge_kernel<64><<<(warps + 7) / 8, 256, 0, stream>>>(p);
+}
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream) {
   if (p.partition / kTT + 1 > kMaxBuckets) return cudaErrorInvalidValue;

@@ -1,0 +1,398 @@
+// decode_mma.cu -- paged decode attention for FP8 (E4M3) KV with 4 or 8 q
+// heads per kv head, on warp-level tensor-core MMAs (sm_103a).
+//
+// Same computation, work decomposition, split plan and merge as decode.cu
+// ("TensorRT-LLM框架解析与高性能推理优化实践" §6.2 paged attention, §6.1 running
+// max / sum, §7.2 KV quantised and dequantised inside the kernel).  With FP8
+// KV and G packed q heads a kv head's token costs 2G multiply-adds per byte,
+// which the CUDA cores cannot sustain at HBM speed; here each warp does the
+// per-tile contractions with mma.sync m16n8k16 (f16 inputs, fp32 accumulate),
+// converting the E4M3 codes to f16 (exactly) in registers.
+//
+// Per 16-token tile (one warp, lane = 4 r + c):
+//   QK  S^T[16 tokens x 8 heads] = K[16 x 128] q^T: M = tokens, N = heads
+//       (padded to 8), K = head_dim in 8 steps of 16.  The reduction index is
+//       permuted consistently in A (K) and B (q) so that step s of lane c
+//       covers head_dim 32c + 4s .. 32c + 4s + 3: each lane reads its 32 bytes
+//       of rows r and r + 8 with two 16-byte loads.
+//   softmax per head over the 16 tokens: the scores of head 2c + {0,1} sit in
+//       the 8 lanes with the same c (xor-4/8/16 butterflies); running max and
+//       sum in the log2 domain; P in f16 (exact running max, so P <= 1).
+//   PV  O^T[128 x 8] += V^T[128 x 16 tokens] P^T: M = head_dim (8 tiles of
+//       16), N = heads, K = tokens.  The M index is permuted so that lane r
+//       owns head_dim 16r .. 16r + 15: its V bytes of tokens 2c, 2c+1,
+//       2c+8, 2c+9 are four 16-byte loads, interleaved pairwise with byte
+//       permutes and converted two at a time.  P's B fragment is the S
+//       accumulator transposed 8x8 at a time with movmatrix.
+// K/V tiles (16 rows x 128 B) arrive by 2-D TMA with 128-byte swizzle into a
+// per-warp 3-stage ring; the swizzle makes both the row reads (QK) and the
+// column reads (PV) free of shared-memory bank conflicts.
+#include "pkv_common.cuh"
+#include "pkv_launch.h"
+#include "pkv_tmap.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;        // head_dim (bytes per FP8 row)
+constexpr int kTT = 16;        // tokens per tile
+constexpr int kNW = 4;         // warps per CTA
+constexpr int kST = 3;         // ring stages per warp
+constexpr int kTileBytes = kTT * kD;  // 2 KB
+constexpr int kN = 8;          // MMA N: packed q heads (padded)
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kOffK = 0;                                    // [NW][ST] K tiles
+constexpr int kOffV = kOffK + kNW * kST * kTileBytes;       // [NW][ST] V tiles
+constexpr int kOffCM = kOffV + kNW * kST * kTileBytes;      // float2 [NW][8] (m, l)
+constexpr int kOffCA = kOffCM + kNW * kN * 8;               // float [NW][8][128]
+constexpr int kOffBar = kOffCA + kNW * kN * kD * 4;         // u64 [NW][ST]
+constexpr int kOffMisc = kOffBar + kNW * kST * 8;           // int [4]
+constexpr int kOffPG = kOffMisc + 16;                       // int [pages of a unit]
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_codes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile
+__device__ __forceinline__ const uint8_t* swz(const uint8_t* tile, int row, int chunk) {
+  return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ int unit_len(int L, int cap, int32_t* err) {
+  if (L < 0 || L > cap) {
+    record_error(err, kDevBadPage);
+    return L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kNW * 32)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  static_assert(G == 4 || G == 8, "4 or 8 q heads per kv head");
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  uint8_t* const kbuf = smem + kOffK + warp * kST * kTileBytes;
+  uint8_t* const vbuf = smem + kOffV + warp * kST * kTileBytes;
+  float2* const cm = reinterpret_cast<float2*>(smem + kOffCM);
+  float* const ca = reinterpret_cast<float*>(smem + kOffCA);
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + kOffBar) + warp * kST;
+  int* const misc = reinterpret_cast<int*>(smem + kOffMisc);
+  int* const pages = reinterpret_cast<int*>(smem + kOffPG);
+  volatile int* const abort_flag = misc + 2;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kST; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    misc[0] = atomicAdd(p.counters + 1, 1);
+    misc[2] = 0;
+  }
+  __syncthreads();
+
+  const int Hkv = p.num_kv_heads, P = p.block_size;
+  const int n_units = p.counters[0] * Hkv;
+  const float qm = p.q_mult;  // scale * k_scale * log2(e)
+  uint32_t jt = 0;            // tiles this warp has consumed
+  int unit = misc[0];
+
+  while (unit < n_units) {
+    int next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(p.counters + 1, 1);
+    const int2 item = p.items[unit / Hkv];
+    const int h = unit - (unit / Hkv) * Hkv;
+    const int s = item.x, k = item.y;
+    const int L = unit_len(__ldg(p.context_lens + s), p.max_len, p.err);
+    const int ns = decode_num_splits(L, p.partition);
+    const int t0 = ns == 1 ? 0 : k * p.partition;
+    const int t1 = ns == 1 ? L : min(L, t0 + p.partition);
+    const int pg0 = t0 / P;
+    const int npg = (t1 - t0 + P - 1) / P;
+    for (int i = threadIdx.x; i < npg; i += kNW * 32) {
+      int pid = __ldg(p.block_tables + size_t(s) * p.max_blocks + pg0 + i);
+      if (pid < 0 || pid >= p.num_blocks) {
+        record_error(p.err, kDevBadPage);
+        pid = -1;
+      }
+      pages[i] = pid;
+    }
+    // B fragments of q for the 8 reduction steps: head g = r (zero past G),
+    // head_dim 32c + 4s + {0,1} and + {2,3}
+    uint32_t qb[16];
+    {
+      const int g = r;
+      if (g < G) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(p.q) +
+            (size_t(s) * p.num_q_heads + size_t(h) * G + g) * kD + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // 8 bf16 = 2 steps per 16-byte load
+          const uint4 u = __ldg(src + i);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = bf16x2_to_float2(w[j]);
+            qb[4 * i + j] = f16x2_of(f.x, f.y);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qb[i] = 0u;
+      }
+    }
+    __syncthreads();  // pages[] visible
+
+    const int ntile = (t1 - t0 + kTT - 1) / kTT;
+    const int my_n = warp < ntile ? (ntile - warp + kNW - 1) / kNW : 0;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // heads 2c, 2c+1
+    float o[8][4];  // O^T m-tile i: rows 16r + 2i (+1), heads 2c, 2c+1
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+
+    auto issue = [&](int j) {  // lane 0: TMA of this warp's j-th tile of the unit
+      const int stage = int((jt + j) % kST);
+      const int ts = t0 + (warp + j * kNW) * kTT;
+      int pid = pages[ts / P - pg0];
+      if (pid < 0) pid = p.num_blocks;  // out of range: zero fill, tile masked
+      mbar_arrive_expect_tx(&bars[stage], 2 * kTileBytes);
+      tma_load_4d(kbuf + stage * kTileBytes, &tm_k, 0, ts % P, h, pid, &bars[stage]);
+      tma_load_4d(vbuf + stage * kTileBytes, &tm_v, 0, ts % P, h, pid, &bars[stage]);
+    };
+    if (lane == 0)
+      for (int j = 0; j < min(kST, my_n); ++j) issue(j);
+
+    for (int j = 0; j < my_n; ++j) {
+      const int stage = int((jt + j) % kST);
+      const uint32_t parity = ((jt + j) / kST) & 1;
+      const int ts = t0 + (warp + j * kNW) * kTT;
+      const int ntok = pages[ts / P - pg0] < 0 ? 0 : min(kTT, t1 - ts);
+      mbar_wait_bounded(&bars[stage], parity, p.err, abort_flag);
+      const uint8_t* kt = kbuf + stage * kTileBytes;
+      const uint8_t* vt = vbuf + stage * kTileBytes;
+
+      // ---- S^T = K q^T ------------------------------------------------------------
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint4 ka = lds128(swz(kt, r, 2 * c)), kb = lds128(swz(kt, r, 2 * c + 1));
+        const uint4 la = lds128(swz(kt, r + 8, 2 * c)), lb = lds128(swz(kt, r + 8, 2 * c + 1));
+        const uint32_t wr[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+        const uint32_t w8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+        for (int st = 0; st < 8; ++st)
+          mma_16816(sacc, e4m3x2_f16x2(wr[st]), e4m3x2_f16x2(w8[st]), e4m3x2_f16x2(wr[st] >> 16),
+                    e4m3x2_f16x2(w8[st] >> 16), qb[2 * st], qb[2 * st + 1]);
+      }
+      // sacc: [0] token r head 2c, [1] token r head 2c+1, [2] token r+8 head 2c,
+      // [3] token r+8 head 2c+1
+      const bool v0 = r < ntok, v1 = r + 8 < ntok;
+      float sv[4] = {v0 ? sacc[0] * qm : -INFINITY, v0 ? sacc[1] * qm : -INFINITY,
+                     v1 ? sacc[2] * qm : -INFINITY, v1 ? sacc[3] * qm : -INFINITY};
+
+      // ---- online softmax per head over the tile's 16 tokens ----------------------
+      float pv[4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float mx = fmaxf(sv[hh], sv[hh + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run[hh], mx);
+        float alpha = 1.f, p0 = 0.f, p1 = 0.f;
+        if (m_new != -INFINITY) {
+          alpha = fast_exp2(m_run[hh] - m_new);
+          p0 = fast_exp2(sv[hh] - m_new);
+          p1 = fast_exp2(sv[hh + 2] - m_new);
+        }
+        float sum = p0 + p1;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        l_run[hh] = l_run[hh] * alpha + sum;
+        m_run[hh] = m_new;
+        pv[hh] = p0;
+        pv[hh + 2] = p1;
+        if (alpha != 1.f) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[i][hh] *= alpha;
+            o[i][hh + 2] *= alpha;
+          }
+        }
+      }
+      // B fragments of P^T: the accumulator rows (tokens) r / r+8 transposed
+      const uint32_t pb0 = movmatrix_trans(f16x2_of(pv[0], pv[1]));
+      const uint32_t pb1 = movmatrix_trans(f16x2_of(pv[2], pv[3]));
+
+      // ---- O^T += V^T P^T -----------------------------------------------------------
+      {
+        uint4 x0 = lds128(swz(vt, 2 * c, r)), x1 = lds128(swz(vt, 2 * c + 1, r));
+        uint4 y0 = lds128(swz(vt, 2 * c + 8, r)), y1 = lds128(swz(vt, 2 * c + 9, r));
+        if (ntok < kTT) {  // rows past the tile end: zero (never-written slots may hold NaN)
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          if (2 * c >= ntok) x0 = z;
+          if (2 * c + 1 >= ntok) x1 = z;
+          if (2 * c + 8 >= ntok) y0 = z;
+          if (2 * c + 9 >= ntok) y1 = z;
+        }
+        const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
+        const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // bytes 4q..4q+3 of each row = head_dim 16r + 4q .. + 3 = m-tiles 2q, 2q+1
+          const uint32_t e = __byte_perm(X0[q], X1[q], 0x5140);
+          const uint32_t f = __byte_perm(X0[q], X1[q], 0x7362);
+          const uint32_t ey = __byte_perm(Y0[q], Y1[q], 0x5140);
+          const uint32_t fy = __byte_perm(Y0[q], Y1[q], 0x7362);
+          mma_16816(o[2 * q], e4m3x2_f16x2(e), e4m3x2_f16x2(e >> 16), e4m3x2_f16x2(ey),
+                    e4m3x2_f16x2(ey >> 16), pb0, pb1);
+          mma_16816(o[2 * q + 1], e4m3x2_f16x2(f), e4m3x2_f16x2(f >> 16), e4m3x2_f16x2(fy),
+                    e4m3x2_f16x2(fy >> 16), pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && j + kST < my_n) {
+        fence_proxy_async_smem();
+        issue(j + kST);
+      }
+    }
+    jt += uint32_t(my_n);
+
+    // ---- combine the warps ---------------------------------------------------------
+    if (r == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        if (2 * c + hh < G) cm[warp * G + 2 * c + hh] = make_float2(m_run[hh], l_run[hh]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int g = 2 * c + (e & 1), d = 16 * r + 2 * i + (e >> 1);
+        if (g < G) ca[(warp * G + g) * kD + d] = o[i][e];
+      }
+    if (threadIdx.x == 0) misc[1] = next;
+    __syncthreads();
+    const int next_unit = misc[1];
+    for (int idx = threadIdx.x; idx < G * kD; idx += kNW * 32) {
+      const int g = idx / kD, d = idx - g * kD;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) M = fmaxf(M, cm[w * G + g].x);
+      float lsum = 0.f, a = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) {
+          const float2 ml = cm[w * G + g];
+          const float sw = fast_exp2(ml.x - M);
+          lsum = fmaf(sw, ml.y, lsum);
+          a = fmaf(sw, ca[(w * G + g) * kD + d], a);
+        }
+      }
+      const size_t row = size_t(s) * p.num_q_heads + size_t(h) * G + g;
+      if (ns == 1) {
+        const float out = lsum > 0.f ? a / lsum * p.v_mult : 0.f;
+        static_cast<__nv_bfloat16*>(p.out)[row * kD + d] = __float2bfloat16_rn(out);
+      } else {
+        const size_t prow = row * p.max_splits + k;
+        p.ws_acc[prow * kD + d] = a;
+        if (d == 0) reinterpret_cast<float2*>(p.ws_ml)[prow] = make_float2(M, lsum);
+      }
+    }
+    __syncthreads();  // shared state is reused by the next unit
+    unit = next_unit;
+  }
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                     int num_sms, cudaStream_t stream) {
+  auto kern = decode_mma_kernel<G>;
+  const int max_pages = (p.partition + p.block_size - 1) / p.block_size + 1;
+  const int smem = kOffPG + 4 * max_pages + 16 + 1024;  // + alignment slack
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  launch_decode_plan(p, stream);
+  kern<<<num_sms * per_sm, kNW * 32, smem, stream>>>(tk, tv, p);
+  if (p.max_splits > 1) launch_decode_merge(p, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (p.head_dim != kD || (G != 4 && G != 8) || kTT > p.block_size) return cudaErrorNotSupported;
+  if (p.num_blocks >= (1 << 30)) return cudaErrorInvalidValue;
+  // pools as bytes [num_blocks][Hkv][P][128]; one box = 16 rows of one page
+  const uint64_t P = p.block_size, Hkv = p.num_kv_heads;
+  CUtensorMap tk, tv;
+  const auto kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (!make_map_4d(&tk, kU8, p.k_pool, kD, P, Hkv, uint64_t(p.num_blocks), kD, P * kD,
+                   Hkv * P * kD, kD, kTT, 1, 1))
+    return cudaErrorInvalidValue;
+  if (!make_map_4d(&tv, kU8, p.v_pool, kD, P, Hkv, uint64_t(p.num_blocks), kD, P * kD,
+                   Hkv * P * kD, kD, kTT, 1, 1))
+    return cudaErrorInvalidValue;
+  return G == 8 ? launch_g<8>(p, tk, tv, num_sms, stream) : launch_g<4>(p, tk, tv, num_sms, stream);
+}
+
+}  // namespace pkv

@@ -40,6 +40,7 @@
 
 #include "pkv_common.cuh"
 #include "pkv_launch.h"
+#include "pkv_tmap.h"
 
 namespace pkv {
 namespace {
@@ -539,36 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---- host: tensor maps ------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 4-D bf16 map: dims (inner first) d0..d3, row strides in bytes for d1..d3.
-bool make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t d3, uint64_t s1, uint64_t s2, uint64_t s3, uint32_t b0, uint32_t b1,
-              uint32_t b2, uint32_t b3) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {d0, d1, d2, d3};
-  const cuuint64_t strides[3] = {s1, s2, s3};
-  const cuuint32_t box[4] = {b0, b1, b2, b3};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
@@ -581,15 +552,16 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
   const uint64_t D = kD, P = p.block_size, Hkv = p.num_kv_heads, E = 2;
   CUtensorMap tq, tk, tv;
   // q [T][Hkv][G][D] with box (64, G, 1, 128/G): rows ordered token-major, head-minor
-  if (!make_map(&tq, p.q, D, G, Hkv, uint64_t(p.num_q_tokens), D * E, G * D * E, Hkv * G * D * E,
-                64, uint32_t(G), 1, uint32_t(kM / G)))
+  const auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map_4d(&tq, kBf16, p.q, D, G, Hkv, uint64_t(p.num_q_tokens), D * E, G * D * E,
+                   Hkv * G * D * E, 64, uint32_t(G), 1, uint32_t(kM / G)))
     return cudaErrorInvalidValue;
   // pools [nb][Hkv][P][D] with box (64, P, 1, 1): one page of one kv head
-  if (!make_map(&tk, k_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E, Hkv * P * D * E,
-                64, uint32_t(P), 1, 1))
+  if (!make_map_4d(&tk, kBf16, k_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
+                   Hkv * P * D * E, 64, uint32_t(P), 1, 1))
     return cudaErrorInvalidValue;
-  if (!make_map(&tv, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E, Hkv * P * D * E,
-                64, uint32_t(P), 1, 1))
+  if (!make_map_4d(&tv, kBf16, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
+                   Hkv * P * D * E, 64, uint32_t(P), 1, 1))
     return cudaErrorInvalidValue;
   static bool configured[64] = {false};
   int dev = 0;

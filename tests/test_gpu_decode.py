@@ -65,7 +65,7 @@ def test_split_partitions_agree_with_oracle(partition):
 
 
 @pytest.mark.parametrize("G,D,P", [(1, 64, 16), (2, 128, 32), (4, 64, 64), (8, 128, 16),
-                                   (8, 64, 32), (1, 128, 64)])
+                                   (8, 64, 32), (1, 128, 64), (4, 128, 64), (8, 128, 32)])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
 def test_shapes_and_ragged_lengths(G, D, P, kv_dtype):
     # lengths around tile (16), page and partition boundaries, plus 0 and 1
@@ -93,14 +93,16 @@ def test_full_block_table_capacity():
     _check_all_rows(w, out)
 
 
-def test_bad_page_id_is_reported_not_dereferenced():
-    w = W.small_config(2)
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_bad_page_id_is_reported_not_dereferenced(cfg):
+    w = W.small_config(cfg)
     d = device_step_inputs(w)
     kp, vp = device_pools(w)
     bt = d["block_tables"].clone()
     bt[1, 2] = w.num_blocks + 1000             # far outside the pool
     bt[2, 0] = -7
-    pkv.paged_attention(d["q"], kp, vp, bt, d["context_lens"], w.max_context_len, w.scale)
+    pkv.paged_attention(d["q"], kp, vp, bt, d["context_lens"], w.max_context_len, w.scale,
+                        k_scale=w.k_scale, v_scale=w.v_scale)
     assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_BOUNDS
     # a clean call afterwards is unaffected
     out = _run_step(w, d, kp, vp)
