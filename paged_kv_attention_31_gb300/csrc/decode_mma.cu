@@ -25,7 +25,7 @@
 //       permutes and converted two at a time.  P's B fragment is the S
 //       accumulator transposed 8x8 at a time with movmatrix.
 // K/V tiles (16 rows x 128 B) arrive by 2-D TMA with 128-byte swizzle into a
-// per-warp 3-stage ring; the swizzle makes both the row reads (QK) and the
+// per-warp 2-stage ring; the swizzle makes both the row reads (QK) and the
 // column reads (PV) free of shared-memory bank conflicts.
 #include "pkv_common.cuh"
 #include "pkv_launch.h"
@@ -37,7 +37,10 @@ namespace {
 constexpr int kD = 128;        // head_dim (bytes per FP8 row)
 constexpr int kTT = 16;        // tokens per tile
 constexpr int kNW = 4;         // warps per CTA
-constexpr int kST = 3;         // ring stages per warp
+#ifndef PKV_MMA_STAGES
+#define PKV_MMA_STAGES 2
+#endif
+constexpr int kST = PKV_MMA_STAGES;  // ring stages per warp
 constexpr int kTileBytes = kTT * kD;  // 2 KB
 constexpr int kN = 8;          // MMA N: packed q heads (padded)
 // shared memory layout (offsets from a 1024-aligned base)
@@ -217,16 +220,23 @@ __global__ void __launch_bounds__(kNW * 32)
       const uint8_t* vt = vbuf + stage * kTileBytes;
 
       // ---- S^T = K q^T ------------------------------------------------------------
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two independent accumulator chains (even / odd reduction steps)
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const uint4 ka = lds128(swz(kt, r, 2 * c)), kb = lds128(swz(kt, r, 2 * c + 1));
         const uint4 la = lds128(swz(kt, r + 8, 2 * c)), lb = lds128(swz(kt, r + 8, 2 * c + 1));
         const uint32_t wr[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
         const uint32_t w8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-        for (int st = 0; st < 8; ++st)
+        for (int st = 0; st < 8; st += 2) {
           mma_16816(sacc, e4m3x2_f16x2(wr[st]), e4m3x2_f16x2(w8[st]), e4m3x2_f16x2(wr[st] >> 16),
                     e4m3x2_f16x2(w8[st] >> 16), qb[2 * st], qb[2 * st + 1]);
+          mma_16816(sacc2, e4m3x2_f16x2(wr[st + 1]), e4m3x2_f16x2(w8[st + 1]),
+                    e4m3x2_f16x2(wr[st + 1] >> 16), e4m3x2_f16x2(w8[st + 1] >> 16),
+                    qb[2 * st + 2], qb[2 * st + 3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
       }
       // sacc: [0] token r head 2c, [1] token r head 2c+1, [2] token r+8 head 2c,
       // [3] token r+8 head 2c+1
