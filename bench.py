@@ -59,7 +59,9 @@ def _ncu_traffic(kernel, workload_name):
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    want = _src_hash("decode.cu" if kernel == "decode_kernel" else "prefill.cu")
+    src = {"decode_kernel": "decode.cu", "decode_mma_kernel": "decode_mma.cu",
+           "prefill_kernel": "prefill.cu"}[kernel]
+    want = _src_hash(src)
     for line in open(path):
         m = re.match(r"\s*-\s*traffic:\s*(\S+)\s+(\S+)\s+bytes_per_launch=(\d+)\s+src=(\w+)", line)
         if m and m.group(1) == kernel and m.group(2) == workload_name and m.group(4) == want:
@@ -389,6 +391,9 @@ def run_gpu(args):
                              // w.block_size)) * 4 + B * 4)
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
+    # FP8 KV with 4 or 8 q heads per kv head at head_dim 128 runs on the MMA decode
+    kname = ("decode_mma_kernel" if w.kv_dtype == "fp8_e4m3" and D == 128 and w.group in (4, 8)
+             else "decode_kernel")
     launches_per_step = 3 + (1 if has_prefill else 0)   # append, plan, decode (+ prefill)
     part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,
                                                 w.k_scale, w.v_scale)
@@ -403,9 +408,9 @@ def run_gpu(args):
         "frac_of_hbm_peak": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "decode_kernel (pkv_paged_attention: plan + decode + merge)",
+                     "kernel": f"{kname} (pkv_paged_attention: plan + decode + merge)",
                      "algorithmic_bytes_per_launch": attn_bytes,
-                     "traffic": _ncu_traffic("decode_kernel", w.name)},
+                     "traffic": _ncu_traffic(kname, w.name)},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -68,11 +68,16 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-// Two E4M3 codes (low byte first) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_codes) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return uint32_t(h.x) | (uint32_t(h.y) << 16);
+// Four E4M3 codes (bytes 0..3 of w) -> f16x2 (b0, b1) and (b2, b3), exact;
+// the lower byte of each pair lands in the lower half.  One cvt per pair, no
+// repacking.
+__device__ __forceinline__ void e4m3x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
@@ -228,12 +233,11 @@ __global__ void __launch_bounds__(kNW * 32)
         const uint32_t wr[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
         const uint32_t w8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-        for (int st = 0; st < 8; st += 2) {
-          mma_16816(sacc, e4m3x2_f16x2(wr[st]), e4m3x2_f16x2(w8[st]), e4m3x2_f16x2(wr[st] >> 16),
-                    e4m3x2_f16x2(w8[st] >> 16), qb[2 * st], qb[2 * st + 1]);
-          mma_16816(sacc2, e4m3x2_f16x2(wr[st + 1]), e4m3x2_f16x2(w8[st + 1]),
-                    e4m3x2_f16x2(wr[st + 1] >> 16), e4m3x2_f16x2(w8[st + 1] >> 16),
-                    qb[2 * st + 2], qb[2 * st + 3]);
+        for (int st = 0; st < 8; ++st) {
+          uint32_t a0, a1, a2, a3;  // rows r / r+8, head_dim 32c + 4st + {0,1} / {2,3}
+          e4m3x4_f16x2(wr[st], a0, a2);
+          e4m3x4_f16x2(w8[st], a1, a3);
+          mma_16816((st & 1) ? sacc2 : sacc, a0, a1, a2, a3, qb[2 * st], qb[2 * st + 1]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
@@ -299,10 +303,13 @@ __global__ void __launch_bounds__(kNW * 32)
           const uint32_t f = __byte_perm(X0[q], X1[q], 0x7362);
           const uint32_t ey = __byte_perm(Y0[q], Y1[q], 0x5140);
           const uint32_t fy = __byte_perm(Y0[q], Y1[q], 0x7362);
-          mma_16816(o[2 * q], e4m3x2_f16x2(e), e4m3x2_f16x2(e >> 16), e4m3x2_f16x2(ey),
-                    e4m3x2_f16x2(ey >> 16), pb0, pb1);
-          mma_16816(o[2 * q + 1], e4m3x2_f16x2(f), e4m3x2_f16x2(f >> 16), e4m3x2_f16x2(fy),
-                    e4m3x2_f16x2(fy >> 16), pb0, pb1);
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_f16x2(e, a0, a1);
+          e4m3x4_f16x2(ey, a2, a3);
+          mma_16816(o[2 * q], a0, a1, a2, a3, pb0, pb1);
+          e4m3x4_f16x2(f, a0, a1);
+          e4m3x4_f16x2(fy, a2, a3);
+          mma_16816(o[2 * q + 1], a0, a1, a2, a3, pb0, pb1);
         }
       }
       __syncwarp();
