@@ -391,8 +391,8 @@ def run_gpu(args):
                              // w.block_size)) * 4 + B * 4)
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
-    # FP8 KV with 4 or 8 q heads per kv head at head_dim 128 runs on the MMA decode
-    kname = ("decode_mma_kernel" if w.kv_dtype == "fp8_e4m3" and D == 128 and w.group in (4, 8)
+    # 4 or 8 q heads per kv head at head_dim 128 run on the tensor-core decode
+    kname = ("decode_mma_kernel" if D == 128 and w.group in (4, 8) and w.block_size >= 16
              else "decode_kernel")
     launches_per_step = 3 + (1 if has_prefill else 0)   # append, plan, decode (+ prefill)
     part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,

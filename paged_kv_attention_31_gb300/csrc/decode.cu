@@ -521,10 +521,12 @@ namespace {
 
 template <int D, int G, bool FP8>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  // FP8 KV with 4-8 packed q heads: the per-token work (G multiply-adds per
-  // byte for QK and again for PV) outruns the CUDA cores; it runs on
-  // warp-level tensor-core MMAs instead (decode_mma.cu)
-  if constexpr (FP8 && D == 128 && (G == 4 || G == 8)) return launch_decode_mma(p, num_sms, stream);
+  // 4-8 packed q heads: the per-token work (G multiply-adds per element for
+  // QK and again for PV) outruns the CUDA cores; it runs on warp-level
+  // tensor-core MMAs instead (decode_mma.cu)
+  if constexpr (D == 128 && (G == 4 || G == 8)) {
+    if (p.block_size >= 16) return launch_decode_mma(p, FP8, num_sms, stream);
+  }
   constexpr int ST = PKV_DECODE_STAGES;
   using C = DecodeCfg<D, G, FP8, ST>;
   auto kern = decode_kernel<D, G, FP8, ST>;

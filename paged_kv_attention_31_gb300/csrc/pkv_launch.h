@@ -84,8 +84,8 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
 // split planner and partial merge of the decode (decode.cu)
 void launch_decode_plan(const DecodeParams& p, cudaStream_t stream);
 void launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
-// FP8 KV, head_dim 128, 4 or 8 q heads per kv head (decode_mma.cu)
-cudaError_t launch_decode_mma(const DecodeParams& p, int num_sms, cudaStream_t stream);
+// head_dim 128, 4 or 8 q heads per kv head, bf16 or FP8 KV (decode_mma.cu)
+cudaError_t launch_decode_mma(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);
 // Returns cudaErrorNotSupported for shapes without a kernel instance.
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
