@@ -268,7 +268,8 @@ def _config(w, args):
          "mean_context_len": float(np.mean(w.context_lens)), "num_blocks": w.num_blocks,
          "partition_tokens": args.partition or "auto",
          "l2": "no flush: each step streams the whole KV set, far larger than the 129 MB L2",
-         "parallelism": f"replicas x{args.gpus}"}
+         "parallelism": f"replicas x{args.gpus}",
+         "launch": "cuda_graph_replay" if args.graph else "eager"}
     if w.num_prefill:
         c["prefill_chunks"] = [int(x) for x in w.prefill_chunk_lens]
     return c
@@ -332,6 +333,23 @@ def run_gpu(args):
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
+    graph = None
+    if args.graph:
+        # the whole step captured once and replayed (per-kernel timing for the
+        # roofline then comes from a short eager loop below)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(*args_dev)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(*args_dev)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
     # --- timed region: device-resident inputs -------------------------------------
     evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
            for _ in range(args.steps)]
@@ -344,9 +362,16 @@ def run_gpu(args):
     t_stop = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(*args_dev, ev=evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(*args_dev, ev=evs[i])
     t_stop.record(stream)
     torch.cuda.synchronize(dev)
+    if graph is not None:  # per-call event timing from an eager pass
+        for i in range(args.steps):
+            step(*args_dev, ev=evs[i])
+        torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
@@ -444,6 +469,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition tokens (0 = library's automatic choice)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the step in a CUDA graph and time its replays")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="keep only the first N sequences (a smaller case, for profiling)")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)

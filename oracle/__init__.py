@@ -63,15 +63,15 @@ def lib():
             L.pkvo_e4m3_value_array.argtypes = [p, i64, p]
             L.pkvo_kv_append.restype = i32
             L.pkvo_kv_append.argtypes = [p, p, p, i32, i32, i32, i32, i64, i32,
-                                         f32, f32, p, p]
+                                         f32, f32, p, p, p, p]
             L.pkvo_attention_one.restype = i32
             L.pkvo_attention_one.argtypes = [p, p, p, i32, f32, f32, i64, i32, i32,
                                              i32, i32, p, i32, f64, p]
             L.pkvo_paged_attention.restype = i32
-            L.pkvo_paged_attention.argtypes = [p, p, p, i32, f32, f32, i64, i32, i32,
+            L.pkvo_paged_attention.argtypes = [p, p, p, i32, f32, f32, p, p, i64, i32, i32,
                                                i32, p, i32, p, i32, i32, f64, p]
             L.pkvo_paged_attention_rows.restype = i32
-            L.pkvo_paged_attention_rows.argtypes = [p, p, p, i32, f32, f32, i64, i32,
+            L.pkvo_paged_attention_rows.argtypes = [p, p, p, i32, f32, f32, p, p, i64, i32,
                                                     i32, i32, p, i32, p, i32, p, p,
                                                     i32, f64, p]
             L.pkvo_paged_prefill.restype = i32
@@ -85,6 +85,16 @@ def _ptr(a: np.ndarray):
     if not a.flags["C_CONTIGUOUS"]:
         raise ValueError("array must be C-contiguous")
     return ctypes.c_void_p(a.ctypes.data)
+
+
+def _scales(arr, hkv):
+    """Optional per-kv-head scales -> (keepalive array, pointer or None)."""
+    if arr is None:
+        return None, None
+    a = np.ascontiguousarray(arr, dtype=np.float32)
+    if a.shape != (hkv,):
+        raise ValueError("per-head scales must have one entry per kv head")
+    return a, _ptr(a)
 
 
 def _dtype_code(kv_dtype: str) -> int:
@@ -124,8 +134,10 @@ def quantize_bf16(bits: int, scale: float) -> int:
 
 # ---- kv_append -------------------------------------------------------------
 def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, kv_dtype="bf16",
-              k_scale=1.0, v_scale=1.0) -> int:
-    """Scatter new tokens into the pools in place; returns #out-of-pool slots."""
+              k_scale=1.0, v_scale=1.0, k_scales=None, v_scales=None) -> int:
+    """Scatter new tokens into the pools in place; returns #out-of-pool slots.
+
+    FP8: k_scales / v_scales (one per kv head) override k_scale / v_scale."""
     _check_pool(k_pool, kv_dtype)
     _check_pool(v_pool, kv_dtype)
     k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
@@ -134,14 +146,17 @@ def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, kv_dtype="bf16",
     nb, hkv, P, D = k_pool.shape
     T = slots.shape[0]
     assert k_new.shape == (T, hkv, D) and v_new.shape == (T, hkv, D)
+    ka, kptr = _scales(k_scales, hkv)
+    va, vptr = _scales(v_scales, hkv)
     return lib().pkvo_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slots), T, hkv, P, D,
-                                nb, _dtype_code(kv_dtype), k_scale, v_scale,
+                                nb, _dtype_code(kv_dtype), k_scale, v_scale, kptr, vptr,
                                 _ptr(k_pool), _ptr(v_pool))
 
 
 # ---- attention ---------------------------------------------------------------
 def paged_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
-                    kv_dtype="bf16", k_scale=1.0, v_scale=1.0) -> np.ndarray:
+                    kv_dtype="bf16", k_scale=1.0, v_scale=1.0, k_scales=None,
+                    v_scales=None) -> np.ndarray:
     """fp64 out [B, Hq, D] for every (sequence, q head)."""
     _check_pool(k_pool, kv_dtype)
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -151,8 +166,11 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
     B, Hq, Dq = q.shape
     assert Dq == D and Hq % hkv == 0 and bt.shape[0] == B and cl.shape == (B,)
     out = np.zeros((B, Hq, D), dtype=np.float64)
+    ka, kptr = _scales(k_scales, hkv)
+    va, vptr = _scales(v_scales, hkv)
     bad = lib().pkvo_paged_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool),
-                                     _dtype_code(kv_dtype), k_scale, v_scale, nb, hkv,
+                                     _dtype_code(kv_dtype), k_scale, v_scale, kptr, vptr,
+                                     nb, hkv,
                                      P, D, _ptr(bt), bt.shape[1], _ptr(cl), B, Hq,
                                      float(scale), _ptr(out))
     if bad:
@@ -162,7 +180,7 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
 
 def paged_attention_rows(q, k_pool, v_pool, block_tables, context_lens, scale,
                          seq_ids, head_ids, kv_dtype="bf16", k_scale=1.0,
-                         v_scale=1.0) -> np.ndarray:
+                         v_scale=1.0, k_scales=None, v_scales=None) -> np.ndarray:
     """fp64 out [n, D] for the listed (sequence, q head) pairs."""
     _check_pool(k_pool, kv_dtype)
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -173,8 +191,11 @@ def paged_attention_rows(q, k_pool, v_pool, block_tables, context_lens, scale,
     nb, hkv, P, D = k_pool.shape
     Hq = q.shape[1]
     out = np.zeros((si.shape[0], D), dtype=np.float64)
+    ka, kptr = _scales(k_scales, hkv)
+    va, vptr = _scales(v_scales, hkv)
     bad = lib().pkvo_paged_attention_rows(_ptr(q), _ptr(k_pool), _ptr(v_pool),
-                                          _dtype_code(kv_dtype), k_scale, v_scale, nb,
+                                          _dtype_code(kv_dtype), k_scale, v_scale, kptr,
+                                          vptr, nb,
                                           hkv, P, D, _ptr(bt), bt.shape[1], _ptr(cl),
                                           Hq, _ptr(si), _ptr(hi), si.shape[0],
                                           float(scale), _ptr(out))

@@ -17,7 +17,8 @@
  *     the oracle uses the plain two-pass max-subtracted softmax, which the
  *     running form equals.
  *   - §7.2 "KV Cache量化": quantised KV is dequantised inside the attention
- *     ("零拷贝反量化"); here with per-tensor scales: value = e4m3(code)*scale.
+ *     ("零拷贝反量化"): value = e4m3(code) * scale, with one scale per tensor
+ *     or, as the section describes, one scale per attention (kv) head.
  *   - §5.3 "分块上下文处理": a long prompt is processed in chunks; token i of
  *     a chunk of C tokens appended to a sequence of final length L sits at
  *     position L - C + i and attends to keys 0 .. L - C + i.
@@ -124,10 +125,13 @@ static double kv_value(const void *pool, int kv_dtype, int64_t idx, float scale)
 
 /* Store token t's K and V rows (all kv heads) at slot_mapping[t]:
  * page = slot / P, offset = slot % P.  Negative slots are skipped.  Returns
- * the number of tokens whose slot lies beyond the pool (also skipped). */
+ * the number of tokens whose slot lies beyond the pool (also skipped).
+ * FP8: kv head h is quantised with k_scales[h] / v_scales[h] when those
+ * arrays are given, else with k_scale / v_scale. */
 int pkvo_kv_append(const uint16_t *k_new, const uint16_t *v_new,
                    const int64_t *slot_mapping, int T, int Hkv, int P, int D,
                    int64_t num_blocks, int kv_dtype, float k_scale, float v_scale,
+                   const float *k_scales, const float *v_scales,
                    void *k_pool, void *v_pool)
 {
     int bad = 0;
@@ -141,6 +145,8 @@ int pkvo_kv_append(const uint16_t *k_new, const uint16_t *v_new,
         }
         int64_t page = slot / P, off = slot % P;
         for (int h = 0; h < Hkv; h++) {
+            float ks = k_scales ? k_scales[h] : k_scale;
+            float vs = v_scales ? v_scales[h] : v_scale;
             for (int d = 0; d < D; d++) {
                 int64_t src = ((int64_t)t * Hkv + h) * D + d;
                 int64_t dst = ((page * Hkv + h) * P + off) * D + d;
@@ -148,8 +154,8 @@ int pkvo_kv_append(const uint16_t *k_new, const uint16_t *v_new,
                     ((uint16_t *)k_pool)[dst] = k_new[src];
                     ((uint16_t *)v_pool)[dst] = v_new[src];
                 } else {
-                    ((uint8_t *)k_pool)[dst] = pkvo_quantize_bf16(k_new[src], k_scale);
-                    ((uint8_t *)v_pool)[dst] = pkvo_quantize_bf16(v_new[src], v_scale);
+                    ((uint8_t *)k_pool)[dst] = pkvo_quantize_bf16(k_new[src], ks);
+                    ((uint8_t *)v_pool)[dst] = pkvo_quantize_bf16(v_new[src], vs);
                 }
             }
         }
@@ -211,9 +217,11 @@ int pkvo_attention_one(const uint16_t *q_row, const void *k_pool,
 /* ---- decode: every (sequence, q head) ------------------------------------ */
 
 /* q [B][Hq][D] bf16, block_tables [B][max_blocks], context_lens [B],
- * out [B][Hq][D] fp64.  Returns the number of rows with a bad page id. */
+ * out [B][Hq][D] fp64.  FP8 scales per kv head when k_scales / v_scales are
+ * given.  Returns the number of rows with a bad page id. */
 int pkvo_paged_attention(const uint16_t *q, const void *k_pool, const void *v_pool,
                          int kv_dtype, float k_scale, float v_scale,
+                         const float *k_scales, const float *v_scales,
                          int64_t num_blocks, int Hkv, int P, int D,
                          const int32_t *block_tables, int max_blocks,
                          const int32_t *context_lens, int B, int Hq,
@@ -223,7 +231,8 @@ int pkvo_paged_attention(const uint16_t *q, const void *k_pool, const void *v_po
     for (int s = 0; s < B; s++)
         for (int a = 0; a < Hq; a++)
             bad += pkvo_attention_one(q + ((int64_t)s * Hq + a) * D, k_pool, v_pool,
-                                      kv_dtype, k_scale, v_scale, num_blocks, Hkv, P,
+                                      kv_dtype, k_scales ? k_scales[a / G] : k_scale,
+                                      v_scales ? v_scales[a / G] : v_scale, num_blocks, Hkv, P,
                                       D, a / G, block_tables + (int64_t)s * max_blocks,
                                       context_lens[s], scale,
                                       out + ((int64_t)s * Hq + a) * D) != 0;
@@ -233,7 +242,8 @@ int pkvo_paged_attention(const uint16_t *q, const void *k_pool, const void *v_po
 /* Selected (sequence, q head) rows only: out [n][D]. */
 int pkvo_paged_attention_rows(const uint16_t *q, const void *k_pool,
                               const void *v_pool, int kv_dtype, float k_scale,
-                              float v_scale, int64_t num_blocks, int Hkv, int P,
+                              float v_scale, const float *k_scales,
+                              const float *v_scales, int64_t num_blocks, int Hkv, int P,
                               int D, const int32_t *block_tables, int max_blocks,
                               const int32_t *context_lens, int Hq,
                               const int32_t *seq_ids, const int32_t *head_ids,
@@ -243,7 +253,8 @@ int pkvo_paged_attention_rows(const uint16_t *q, const void *k_pool,
     for (int r = 0; r < n; r++) {
         int s = seq_ids[r], a = head_ids[r];
         bad += pkvo_attention_one(q + ((int64_t)s * Hq + a) * D, k_pool, v_pool,
-                                  kv_dtype, k_scale, v_scale, num_blocks, Hkv, P, D,
+                                  kv_dtype, k_scales ? k_scales[a / G] : k_scale,
+                                  v_scales ? v_scales[a / G] : v_scale, num_blocks, Hkv, P, D,
                                   a / G, block_tables + (int64_t)s * max_blocks,
                                   context_lens[s], scale, out + (int64_t)r * D) != 0;
     }

@@ -276,3 +276,70 @@ def test_kv_append_fp8_matches_torch_quantisation():
         want = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         got = _slots_view(pool)[slots]
         assert np.array_equal(got, want)
+
+
+# ---- per-head FP8 scales ("KV Cache量化": one scale per attention head) ----
+def test_kv_append_fp8_per_head_scales_match_torch():
+    rng = np.random.default_rng(40)
+    nb, hkv, P, D, T = 6, 3, 4, 16, 11
+    kp = np.zeros((nb, hkv, P, D), np.uint8)
+    vp = np.zeros_like(kp)
+    slots = rng.choice(nb * P, T, replace=False).astype(np.int64)
+    kn = _rand_bf16(rng, (T, hkv, D), 2.0)
+    vn = _rand_bf16(rng, (T, hkv, D), 0.5)
+    ks = np.array([0.031, 0.0517, 0.09], np.float32)
+    vs = np.array([0.0077, 0.0093, 0.021], np.float32)
+    oracle.kv_append(kn, vn, slots, kp, vp, "fp8_e4m3", 1.0, 1.0, k_scales=ks, v_scales=vs)
+    for new, pool, sc in ((kn, kp, ks), (vn, vp, vs)):
+        x = (new.astype(np.uint32) << 16).view(np.float32)          # [T, hkv, D]
+        y = torch.from_numpy(x) / torch.from_numpy(sc)[None, :, None]
+        assert float(y.abs().max()) <= 448
+        want = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(_slots_view(pool)[slots], want)
+
+
+def test_fp8_per_head_scales_match_dense_dequantised():
+    D, P, Hkv, Hq = 16, 4, 2, 6
+    rng = np.random.default_rng(41)
+    lens = [9, 14]
+    codes = lambda n: rng.integers(0, 256, (n, Hkv, D)).astype(np.uint8)
+    Kc = [codes(L) for L in lens]
+    Vc = [codes(L) for L in lens]
+    for x in Kc + Vc:
+        x[(x & 0x7F) == 0x7F] = 0x7E
+    kp, bt = paginate(Kc, P, 10, np.random.default_rng(6), np.uint8)
+    vp, _ = paginate(Vc, P, 10, np.random.default_rng(6), np.uint8)
+    q = _rand_bf16(rng, (2, Hq, D), 0.01)
+    ks = np.array([0.011, 0.004], np.float32)
+    vs = np.array([0.02, 0.05], np.float32)
+    out = oracle.paged_attention(q, kp, vp, bt, np.array(lens, np.int32), 0.25,
+                                 kv_dtype="fp8_e4m3", k_scales=ks, v_scales=vs)
+    deq = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for s, L in enumerate(lens):
+        ref = dense_attention(bf16_to_f64(q[s])[:, None, :],
+                              (deq(Kc[s]) * ks.astype(np.float64)[None, :, None]).transpose(1, 0, 2),
+                              (deq(Vc[s]) * vs.astype(np.float64)[None, :, None]).transpose(1, 0, 2),
+                              0.25)[:, 0, :]
+        np.testing.assert_allclose(out[s], ref, rtol=0, atol=1e-12)
+
+
+def test_equal_per_head_scales_reduce_to_per_tensor():
+    rng = np.random.default_rng(42)
+    nb, hkv, P, D, T = 5, 2, 4, 16, 14
+    slots = rng.choice(nb * P, T, replace=False).astype(np.int64)
+    kn = _rand_bf16(rng, (T, hkv, D))
+    vn = _rand_bf16(rng, (T, hkv, D))
+    a = [np.zeros((nb, hkv, P, D), np.uint8) for _ in range(4)]
+    oracle.kv_append(kn, vn, slots, a[0], a[1], "fp8_e4m3", 0.013, 0.021)
+    oracle.kv_append(kn, vn, slots, a[2], a[3], "fp8_e4m3", 9.0, 9.0,
+                     k_scales=np.full(hkv, 0.013, np.float32),
+                     v_scales=np.full(hkv, 0.021, np.float32))
+    assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
+    bt = np.arange(nb, dtype=np.int32)[None]
+    q = _rand_bf16(rng, (1, 4, D))
+    cl = np.array([nb * P], np.int32)
+    x = oracle.paged_attention(q, a[0], a[1], bt, cl, 0.25, "fp8_e4m3", 0.013, 0.021)
+    y = oracle.paged_attention(q, a[0], a[1], bt, cl, 0.25, "fp8_e4m3", 7.0, 7.0,
+                               k_scales=np.full(hkv, 0.013, np.float32),
+                               v_scales=np.full(hkv, 0.021, np.float32))
+    assert np.array_equal(x, y)
