@@ -67,7 +67,12 @@ typedef enum pkv_kv_dtype {
 } pkv_kv_dtype;
 
 /* Shape of the paged pool.  head_dim in {64, 128}; block_size in
- * {16, 32, 64}; k_scale / v_scale (> 0, finite) are used only for FP8. */
+ * {16, 32, 64}.  FP8 only: one scale per tensor (k_scale / v_scale, > 0 and
+ * finite), or one per kv head as the page's KV-cache quantisation section
+ * describes (§7.2 "为每个attention head单独计算scale"): k_scales / v_scales,
+ * optional device arrays of num_kv_heads positive finite floats (4-byte
+ * aligned) that override the scalars when non-NULL.  Values in those arrays
+ * are device data and are not checked. */
 typedef struct pkv_pool_desc {
     int32_t num_blocks;
     int32_t num_kv_heads;
@@ -76,6 +81,8 @@ typedef struct pkv_pool_desc {
     int32_t kv_dtype;          /* pkv_kv_dtype */
     float k_scale;
     float v_scale;
+    const float *k_scales;     /* optional, device [num_kv_heads] */
+    const float *v_scales;     /* optional, device [num_kv_heads] */
 } pkv_pool_desc;
 
 /*
@@ -90,7 +97,8 @@ typedef struct pkv_pool_desc {
  *   k_pool, v_pool device pools (see layout above), 16-byte aligned
  *   pool           host descriptor
  * bf16 pools store the bits unchanged.  FP8 pools store
- * e4m3_rn_satfinite(x / scale), the quotient taken in IEEE binary32.
+ * e4m3_rn_satfinite(x / scale), the quotient taken in IEEE binary32, with
+ * the token's kv head's scale when per-head scales are given.
  * num_tokens == 0 is a no-op.  Two tokens with the same slot race.
  */
 PKV_API pkv_status pkv_kv_append(const void *k_new, const void *v_new,
@@ -134,6 +142,7 @@ PKV_API pkv_status pkv_paged_attention_plan(int32_t num_seqs, int32_t num_q_head
  *   max_context_len host upper bound of context_lens (sizes the split plan)
  *   scale           softmax scale (e.g. 1/sqrt(head_dim)); FP8 scores are
  *                   additionally multiplied by k_scale and outputs by v_scale
+ *                   (those of the kv head, with per-head scales)
  *   partition_tokens split-K partition length in tokens: a sequence longer
  *                   than it is processed as ceil(L/partition) independent
  *                   partitions merged by a second kernel.  0 = automatic.

@@ -50,7 +50,8 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float)]
+                ("v_scale", ctypes.c_float), ("k_scales", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p)]
 
 
 def lib():
@@ -129,23 +130,37 @@ def _is_fp8_pool(pool: torch.Tensor) -> bool:
     raise TypeError("pool must be bfloat16, uint8 or float8_e4m3fn")
 
 
-def pool_desc(k_pool: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> PoolDesc:
-    """Descriptor of a pool tensor [num_blocks, Hkv, block_size, head_dim]."""
+def _scales_ptr(scales: Optional[torch.Tensor], hkv: int):
+    if scales is None:
+        return None
+    if scales.dtype != torch.float32 or scales.numel() != hkv:
+        raise ValueError("per-head scales must be float32 with one entry per kv head")
+    return _ptr(scales).value
+
+
+def pool_desc(k_pool: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0,
+              k_scales: Optional[torch.Tensor] = None,
+              v_scales: Optional[torch.Tensor] = None) -> PoolDesc:
+    """Descriptor of a pool tensor [num_blocks, Hkv, block_size, head_dim].
+
+    FP8 pools: per-tensor scales, or per-kv-head scale tensors (float32 [Hkv]
+    on the device) that override them."""
     if k_pool.dim() != 4:
         raise ValueError("pool must be [num_blocks, num_kv_heads, block_size, head_dim]")
     nb, hkv, P, D = k_pool.shape
     return PoolDesc(nb, hkv, P, D, KV_FP8_E4M3 if _is_fp8_pool(k_pool) else KV_BF16,
-                    float(k_scale), float(v_scale))
+                    float(k_scale), float(v_scale), _scales_ptr(k_scales, hkv),
+                    _scales_ptr(v_scales, hkv))
 
 
 def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale=1.0, v_scale=1.0,
-              stream=None) -> None:
+              stream=None, k_scales=None, v_scales=None) -> None:
     """Write new tokens' K/V rows ([T, Hkv, D] bf16) to their pool slots."""
     if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16:
         raise TypeError("k_new / v_new must be bfloat16")
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
-    desc = pool_desc(k_pool, k_scale, v_scale)
+    desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     if v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
         raise ValueError("k_pool and v_pool differ")
     T = int(slot_mapping.shape[0])
@@ -181,13 +196,13 @@ def paged_attention_plan(num_seqs, num_q_heads, max_context_len, k_pool, partiti
 
 def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale,
                     out=None, workspace=None, k_scale=1.0, v_scale=1.0, partition_tokens=0,
-                    stream=None) -> torch.Tensor:
+                    stream=None, k_scales=None, v_scales=None) -> torch.Tensor:
     """Decode attention: q [B, Hq, D] bf16 -> out [B, Hq, D] bf16."""
     if q.dtype != torch.bfloat16 or q.dim() != 3:
         raise TypeError("q must be bfloat16 [num_seqs, num_q_heads, head_dim]")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables / context_lens must be int32")
-    desc = pool_desc(k_pool, k_scale, v_scale)
+    desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
@@ -207,7 +222,7 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_l
 
 def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_context_len,
                             scale, out=None, k_scale=1.0, v_scale=1.0, partition_tokens=0,
-                            stream=None) -> torch.Tensor:
+                            stream=None, k_scales=None, v_scales=None) -> torch.Tensor:
     """Decode attention without a workspace, for callers that cannot allocate
     device scratch: the library's fixed device array is used instead (calls
     must not overlap on the GPU; the first call on a device does a one-time
@@ -216,7 +231,7 @@ def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_c
         raise TypeError("q must be bfloat16 [num_seqs, num_q_heads, head_dim]")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables / context_lens must be int32")
-    desc = pool_desc(k_pool, k_scale, v_scale)
+    desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)

@@ -281,6 +281,9 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       }
       pages[i] = pid;
     }
+    // per-kv-head FP8 scales fold into the score and output multipliers
+    const float qm_h = p.k_scales ? p.q_mult * __ldg(p.k_scales + h) : p.q_mult;
+    const float vm_h = p.v_scales ? p.v_mult * __ldg(p.v_scales + h) : p.v_mult;
     // q of the G packed heads, pre-scaled into the log2 domain
     float2 q2[G][E / 2];  // (d, d+1) pairs for packed fp32 FMA
     {
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int j = 0; j < C::NCH; ++j)
-          load_q<EC>(qrow + g * D + (c + j * TPT) * EC, p.q_mult,
+          load_q<EC>(qrow + g * D + (c + j * TPT) * EC, qm_h,
                      reinterpret_cast<float*>(&q2[g][j * EC / 2]));
     }
     __syncthreads();  // pages[] visible
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       }
       const size_t row = size_t(s) * p.num_q_heads + size_t(h) * G + g;
       if (ns == 1) {
-        const float o = lsum > 0.f ? a / lsum * p.v_mult : 0.f;
+        const float o = lsum > 0.f ? a / lsum * vm_h : 0.f;
         static_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(o);
       } else {
         const size_t prow = row * p.max_splits + k;
@@ -513,7 +516,9 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   }
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + size_t(gw) * D + lane * DV;
 #pragma unroll
-  for (int e = 0; e < DV; ++e) dst[e] = __float2bfloat16_rn(lsum > 0.f ? a[e] / lsum * p.v_mult : 0.f);
+  const int kvh = (gw - s * p.num_q_heads) / (p.num_q_heads / p.num_kv_heads);
+  const float vm = p.v_scales ? p.v_mult * __ldg(p.v_scales + kvh) : p.v_mult;
+  for (int e = 0; e < DV; ++e) dst[e] = __float2bfloat16_rn(lsum > 0.f ? a[e] / lsum * vm : 0.f);
 }
 
 // ---- host launch ----------------------------------------------------------------

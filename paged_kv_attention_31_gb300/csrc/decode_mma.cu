@@ -175,7 +175,6 @@ __global__ void __launch_bounds__(kNW * 32)
 
   const int Hkv = p.num_kv_heads, P = p.block_size;
   const int n_units = p.counters[0] * Hkv;
-  const float qm = p.q_mult;  // scale * k_scale * log2(e)
   uint32_t jt = 0;            // tiles this warp has consumed
   int unit = misc[0];
   // bf16 PV: lane r owns chunks (r & 3) and (r & 3) + 4 of half (r >> 2)
@@ -193,6 +192,10 @@ __global__ void __launch_bounds__(kNW * 32)
     const int t1 = ns == 1 ? L : min(L, t0 + p.partition);
     const int pg0 = t0 / P;
     const int npg = (t1 - t0 + P - 1) / P;
+    // score multiplier scale * k_scale * log2(e) and output multiplier v_scale,
+    // with the kv head's scales when per-head scales are given
+    const float qm = p.k_scales ? p.q_mult * __ldg(p.k_scales + h) : p.q_mult;
+    const float vm = p.v_scales ? p.v_mult * __ldg(p.v_scales + h) : p.v_mult;
     for (int i = threadIdx.x; i < npg; i += kNW * 32) {
       int pid = __ldg(p.block_tables + size_t(s) * p.max_blocks + pg0 + i);
       if (pid < 0 || pid >= p.num_blocks) {
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kNW * 32)
       }
       const size_t row = size_t(s) * p.num_q_heads + size_t(h) * G + g;
       if (ns == 1) {
-        const float out = lsum > 0.f ? a / lsum * p.v_mult : 0.f;
+        const float out = lsum > 0.f ? a / lsum * vm : 0.f;
         static_cast<__nv_bfloat16*>(p.out)[row * kD + d] = __float2bfloat16_rn(out);
       } else {
         const size_t prow = row * p.max_splits + k;

@@ -62,8 +62,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     const int64_t elem = ((page * p.num_kv_heads + h) * p.block_size + off) * p.head_dim + c * 8;
     const uint4 kx = __ldg(kn + i);
     const uint4 vx = __ldg(vn + i);
-    store_row_chunk<FP8>(static_cast<uint8_t*>(p.k_pool), elem, kx, p.k_scale);
-    store_row_chunk<FP8>(static_cast<uint8_t*>(p.v_pool), elem, vx, p.v_scale);
+    const float ks = (FP8 && p.k_scales) ? __ldg(p.k_scales + h) : p.k_scale;
+    const float vs = (FP8 && p.v_scales) ? __ldg(p.v_scales + h) : p.v_scale;
+    store_row_chunk<FP8>(static_cast<uint8_t*>(p.k_pool), elem, kx, ks);
+    store_row_chunk<FP8>(static_cast<uint8_t*>(p.v_pool), elem, vx, vs);
   }
 }
 

@@ -50,8 +50,12 @@ pkv_status check_pool(const pkv_pool_desc* pool) {
   if (pool->block_size != 16 && pool->block_size != 32 && pool->block_size != 64)
     return PKV_ERR_UNSUPPORTED;
   if (pool->kv_dtype == PKV_KV_FP8_E4M3) {
-    if (!(pool->k_scale > 0.f) || !(pool->v_scale > 0.f) || !isfinite(pool->k_scale) ||
-        !isfinite(pool->v_scale))
+    if (!pool->k_scales && (!(pool->k_scale > 0.f) || !isfinite(pool->k_scale)))
+      return PKV_ERR_INVALID_ARG;
+    if (!pool->v_scales && (!(pool->v_scale > 0.f) || !isfinite(pool->v_scale)))
+      return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(pool->k_scales) & 3) ||
+        (reinterpret_cast<uintptr_t>(pool->v_scales) & 3))
       return PKV_ERR_INVALID_ARG;
   }
   return PKV_OK;
@@ -140,6 +144,9 @@ pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* sl
   p.head_dim = pool->head_dim;
   p.k_scale = pool->k_scale;
   p.v_scale = pool->v_scale;
+  const bool fp8_pool = pool->kv_dtype == PKV_KV_FP8_E4M3;
+  p.k_scales = fp8_pool ? pool->k_scales : nullptr;
+  p.v_scales = fp8_pool ? pool->v_scales : nullptr;
   p.fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
   p.err = dev->err;
   return from_cuda(pkv::launch_kv_append(p, dev->num_sms, static_cast<cudaStream_t>(stream)));
@@ -245,8 +252,11 @@ pkv_status pkv_paged_attention(const void* q, const void* k_pool, const void* v_
   p.max_len = max_len;
   p.partition = part;
   p.max_splits = splits;
-  p.q_mult = scale * (fp8 ? pool->k_scale : 1.0f) * 1.4426950408889634f;
-  p.v_mult = fp8 ? pool->v_scale : 1.0f;
+  // per-head scales multiply in inside the kernels, per kv head
+  p.k_scales = fp8 ? pool->k_scales : nullptr;
+  p.v_scales = fp8 ? pool->v_scales : nullptr;
+  p.q_mult = scale * (fp8 && !p.k_scales ? pool->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_mult = fp8 && !p.v_scales ? pool->v_scale : 1.0f;
   return from_cuda(pkv::launch_decode(p, fp8, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
 

@@ -17,6 +17,8 @@ struct AppendParams {
   int64_t num_slots;            // num_blocks * block_size
   int32_t num_tokens, num_kv_heads, block_size, head_dim;
   float k_scale, v_scale;
+  const float* k_scales;        // optional per-kv-head scales (override the scalars)
+  const float* v_scales;
   int32_t fp8;
   int32_t* err;
 };
@@ -39,8 +41,10 @@ struct DecodeParams {
   int32_t max_len;              // effective cap on context lengths
   int32_t partition;            // tokens per split partition (multiple of block_size)
   int32_t max_splits;
-  float q_mult;                 // scale * k_scale * log2(e)
-  float v_mult;                 // v_scale (FP8) or 1
+  float q_mult;                 // scale * k_scale * log2(e) (k_scale 1 with per-head scales)
+  float v_mult;                 // v_scale (FP8, per tensor) or 1
+  const float* k_scales;        // optional per-kv-head FP8 scales, multiplied in per head
+  const float* v_scales;
 };
 
 struct PrefillParams {

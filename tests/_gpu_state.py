@@ -21,6 +21,7 @@ def device_pools(w: W.Workload, device="cuda"):
         return k, v
     k = torch.empty(shape, dtype=torch.uint8, device=device)
     v = torch.empty(shape, dtype=torch.uint8, device=device)
+    ks, vs = w.scale_tensors(device)
     per_page = w.num_kv_heads * w.block_size * w.head_dim
     chunk = max(1, (1 << 25) // per_page)
     P = w.block_size
@@ -31,7 +32,7 @@ def device_pools(w: W.Workload, device="cuda"):
         kn = rows(w.pool_source("k", ids, device))
         vn = rows(w.pool_source("v", ids, device))
         slots = torch.arange(start * P, stop * P, dtype=torch.int64, device=device)
-        pkv.kv_append(kn, vn, slots, k, v, w.k_scale, w.v_scale)
+        pkv.kv_append(kn, vn, slots, k, v, w.k_scale, w.v_scale, k_scales=ks, v_scales=vs)
     return k, v
 
 
@@ -56,6 +57,7 @@ def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None)
     appended token whose slot falls in these pages."""
     page_ids = np.asarray(page_ids, np.int64)
     P, D = w.block_size, w.head_dim
+    ks, vs = w.head_scales(h)
     n = len(page_ids)
     src = {c: W.bf16_bits(W.pool_values_head(w.seed, c, page_ids, h, w.num_kv_heads, P, D))
            for c in ("k", "v")}
@@ -64,7 +66,7 @@ def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None)
     vp = np.zeros((n, 1, P, D), dt)
     # initial contents: every slot of these pages
     oracle.kv_append(src["k"].reshape(n * P, 1, D), src["v"].reshape(n * P, 1, D),
-                     np.arange(n * P, dtype=np.int64), kp, vp, w.kv_dtype, w.k_scale, w.v_scale)
+                     np.arange(n * P, dtype=np.int64), kp, vp, w.kv_dtype, ks, vs)
     # this step's appends that land in these pages
     slots = w.append_slot_mapping()
     if k_new_h is None:
@@ -77,7 +79,7 @@ def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None)
         sel = np.array(sel)
         mapped = np.array([where[int(slots[t]) // P] * P + int(slots[t]) % P for t in sel], np.int64)
         oracle.kv_append(k_new_h[sel][:, None, :], v_new_h[sel][:, None, :], mapped, kp, vp,
-                         w.kv_dtype, w.k_scale, w.v_scale)
+                         w.kv_dtype, ks, vs)
     return kp, vp
 
 
@@ -91,8 +93,9 @@ def oracle_decode_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
     G = w.group
     q = W.bf16_bits(w.q_decode()[s, h * G:(h + 1) * G, :])[None]
     table = np.arange(max(npg, 1), dtype=np.int32)[None]
+    ks, vs = w.head_scales(h)
     out = oracle.paged_attention(q, kp, vp, table, np.array([L], np.int32), w.scale,
-                                 w.kv_dtype, w.k_scale, w.v_scale)
+                                 w.kv_dtype, ks, vs)
     return out[0]
 
 

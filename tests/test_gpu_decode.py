@@ -21,10 +21,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _run_step(w, d, k_pool, v_pool, partition=0):
-    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], k_pool, v_pool, w.k_scale, w.v_scale)
+    ks, vs = w.scale_tensors(d["q"].device)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], k_pool, v_pool, w.k_scale, w.v_scale,
+                  k_scales=ks, v_scales=vs)
     return pkv.paged_attention(d["q"], k_pool, v_pool, d["block_tables"], d["context_lens"],
                                w.max_context_len, w.scale, k_scale=w.k_scale,
-                               v_scale=w.v_scale, partition_tokens=partition)
+                               v_scale=w.v_scale, partition_tokens=partition,
+                               k_scales=ks, v_scales=vs)
 
 
 def _check_all_rows(w, out, seqs=None, heads=None):
@@ -80,6 +83,31 @@ def test_shapes_and_ragged_lengths(G, D, P, kv_dtype):
     assert pkv.get_device_error() == 0
     assert torch.all(out[0].float() == 0)
     _check_all_rows(w, out, seqs=range(1, len(lens)))
+
+
+@pytest.mark.parametrize("G,D,P", [(8, 128, 32), (4, 128, 16), (2, 128, 32), (8, 64, 16)])
+@pytest.mark.parametrize("partition", [0, 256])
+def test_fp8_per_head_scales(G, D, P, partition):
+    # per-kv-head K and V scales through both decode paths (tensor-core for
+    # D=128 with 4-8 packed heads, CUDA cores otherwise) and through the merge
+    lens = [1, 17, P + 3, 300, 777, 1500]
+    hkv = 4
+    w = W.with_head_scales(W.make_decode(f"heads_G{G}_D{D}_P{P}", 880 + G + D + P, lens,
+                                         hkv * G, hkv, D, P, kv_dtype="fp8_e4m3"))
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _run_step(w, d, kp, vp, partition=partition)
+    assert pkv.get_device_error() == 0
+    _check_all_rows(w, out)
+
+
+def test_fp8_per_head_scales_prefix_sharing_config():
+    w = W.with_head_scales(W.small_config(4))
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _run_step(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check_all_rows(w, out, heads=[0, 3, 7])
 
 
 def test_full_block_table_capacity():

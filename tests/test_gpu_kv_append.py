@@ -41,6 +41,33 @@ def test_kv_append_bit_exact(fp8, hkv, P, D):
     assert np.array_equal(_bits(gv), vp)
 
 
+@pytest.mark.parametrize("hkv,P,D", [(8, 32, 128), (3, 16, 64)])
+def test_kv_append_per_head_scales_bit_exact(hkv, P, D):
+    # FP8 with one K and one V scale per kv head: head h must be divided by
+    # its own scale (a head-index mix-up changes the codes of every token)
+    rng = np.random.default_rng(400 + hkv)
+    nb, T = 29, 401
+    slots = rng.choice(nb * P, T, replace=False).astype(np.int64)
+    slots[::13] = -1
+    kn = bf16_from_f32(rng.standard_normal((T, hkv, D)).astype(np.float32) * 1.7)
+    vn = bf16_from_f32(rng.standard_normal((T, hkv, D)).astype(np.float32) * 0.6)
+    ks = (0.011 * (1.0 + 0.61 * np.arange(hkv))).astype(np.float32)
+    vs = (0.004 * (1.0 + 0.29 * np.arange(hkv))[::-1]).astype(np.float32)
+    init = rng.integers(0, 120, (nb, hkv, P, D)).astype(np.uint8)
+    kp, vp = init.copy(), init.copy()
+    # the scalar scales are deliberately wrong: the arrays must win
+    oracle.kv_append(kn, vn, slots, kp, vp, "fp8_e4m3", 9.0, 9.0, k_scales=ks, v_scales=vs)
+
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+    gk, gv = to_dev(init).clone(), to_dev(init).clone()
+    pkv.kv_append(to_dev(kn).view(torch.bfloat16), to_dev(vn).view(torch.bfloat16),
+                  torch.from_numpy(slots).cuda(), gk, gv, 9.0, 9.0,
+                  k_scales=torch.from_numpy(ks).cuda(), v_scales=torch.from_numpy(vs).cuda())
+    assert pkv.get_device_error() == 0
+    assert np.array_equal(_bits(gk), kp)
+    assert np.array_equal(_bits(gv), vp)
+
+
 def test_fp8_encoder_special_values():
     # saturation, ties, subnormals, signed zeros, every bf16 pattern in range
     bits = np.arange(1 << 16, dtype=np.uint32)

@@ -105,3 +105,15 @@ def test_generator_identical_on_gpu():
     cpu = W.normal_bf16(31002, "k", idx)
     gpu = W.normal_bf16(31002, "k", idx.cuda()).cpu()
     assert torch.equal(cpu.view(torch.int16), gpu.view(torch.int16))
+
+
+def test_head_scales_workload():
+    w = W.with_head_scales(W.small_config(4))
+    assert w.k_scales.dtype == np.float32 and w.k_scales.shape == (w.num_kv_heads,)
+    assert w.head_scales(0) == (float(np.float32(W.FP8_SCALE)), float(np.float32(W.FP8_SCALE)))
+    assert w.head_scales(3)[0] > w.head_scales(3)[1] > w.head_scales(0)[1]
+    ks, vs = w.scale_tensors()
+    assert ks.dtype == torch.float32 and torch.equal(ks, torch.from_numpy(w.k_scales))
+    assert W.small_config(4).scale_tensors() == (None, None)
+    with pytest.raises(ValueError):
+        W.with_head_scales(W.small_config(3))

@@ -173,6 +173,21 @@ class Workload:
     v_scale: float = 1.0
     shared_prefix_tokens: int = 0
     num_sharers: int = 0
+    k_scales: Optional[np.ndarray] = None  # float32 [Hkv]: per-kv-head FP8 scales
+    v_scales: Optional[np.ndarray] = None  # (override k_scale / v_scale when set)
+
+    def head_scales(self, h: int):
+        """(k scale, v scale) that apply to kv head h."""
+        ks = self.k_scale if self.k_scales is None else float(self.k_scales[h])
+        vs = self.v_scale if self.v_scales is None else float(self.v_scales[h])
+        return ks, vs
+
+    def scale_tensors(self, device="cpu"):
+        """Per-head scale arrays as float32 tensors, or (None, None)."""
+        if self.k_scales is None:
+            return None, None
+        return (torch.from_numpy(np.asarray(self.k_scales, np.float32)).to(device),
+                torch.from_numpy(np.asarray(self.v_scales, np.float32)).to(device))
 
     # -- derived sizes ------------------------------------------------------
     @property
@@ -365,6 +380,18 @@ def make_decode(name, seed, lens, Hq, Hkv, D, P, kv_dtype="bf16",
     sc = FP8_SCALE if kv_dtype == "fp8_e4m3" else 1.0
     return Workload(name, seed, Hq, Hkv, D, P, kv_dtype, nb, lens, tables,
                     pl, pc, pt, sc, sc, shared_tokens, num_sharers)
+
+
+def with_head_scales(w: Workload) -> Workload:
+    """The same FP8 workload with a different scale per kv head: head h uses
+    FP8_SCALE * (1 + 0.37 h) for K and FP8_SCALE * (1 + 0.23 h) for V, so no
+    code saturates and heads differ by up to several binades of code range."""
+    if w.kv_dtype != "fp8_e4m3":
+        raise ValueError("per-head scales apply to FP8 pools")
+    h = np.arange(w.num_kv_heads, dtype=np.float64)
+    ks = (FP8_SCALE * (1.0 + 0.37 * h)).astype(np.float32)
+    vs = (FP8_SCALE * (1.0 + 0.23 * h)).astype(np.float32)
+    return dataclasses.replace(w, name=w.name + "_head_scales", k_scales=ks, v_scales=vs)
 
 
 def make_mixed(name, seed, decode_lens, prior_lens, chunk_lens, Hq, Hkv, D, P,
