@@ -8,7 +8,8 @@ merge).  --workload selects another configuration (1..5); configuration 5 adds
 the chunked-prefill call to the step.
 
 Prints ONE JSON line.  `value` = algorithmic bytes of the step / device time
-per step (KV bytes dominate; see the design doc for the byte count).  `e2e` is the
+per step (K/V bytes streamed dominate: 2 * head_dim * element size per token
+and kv head, plus q, out, block-table entries and the appended rows).  `e2e` is the
 same metric through the public API with inputs copied from pinned host memory
 and the output copied back inside the timed region.  --impl reference times
 the fp64 CPU oracle on a bounded sample of the same workload.
@@ -445,12 +446,14 @@ def run_gpu(args):
         flops = w.prefill_flops()
         tpeak = float(peaks["bf16_tflops"])
         tflops = flops / (prefill_ms * 1e-3) / 1e12
-        line["prefill"] = {"kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
-                           "ms": prefill_ms, "flops_per_launch": flops,
-                           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpeak,
-                                        "unit": "TFLOP/s", "frac": tflops / tpeak,
-                                        "peak_kind": peak_kind,
-                                        "traffic": _ncu_traffic("prefill_kernel", w.name)}}
+        # the prefill call is the step's dominant kernel here: it takes the
+        # top-level roofline, the decode call's moves beside it
+        line["decode_roofline"] = line["roofline"]
+        line["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": tpeak,
+                            "unit": "TFLOP/s", "frac": tflops / tpeak, "peak_kind": peak_kind,
+                            "kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
+                            "algorithmic_flops_per_launch": flops, "ms_per_launch": prefill_ms,
+                            "traffic": _ncu_traffic("prefill_kernel", w.name)}
     if cpu_line is not None:
         line["cpu_baseline"] = cpu_line
     if rank == 0:

@@ -6,8 +6,8 @@
  * K/V of every live sequence sit in fixed-size pages of one shared pool
  * (§4.2 "KV缓存管理细节"), a per-sequence block table maps logical pages to
  * physical ones (§6.2 "Paged Attention优化": block_tables
- * [num_seqs, max_blocks]), sequences may share prefix pages (§6.2
- * "共享前缀优化"), the KV cache may be stored quantised and is dequantised
+ * [num_seqs, max_blocks]), sequences may share prefix pages (§6.2, the
+ * list of its optimisations), the KV cache may be stored quantised and is dequantised
  * inside the attention kernel (§7.2 "KV Cache量化"), and long prompts are
  * processed as chunks interleaved with decode requests (§5.3 "分块上下文处理").
  *
@@ -69,7 +69,7 @@ typedef enum pkv_kv_dtype {
 /* Shape of the paged pool.  head_dim in {64, 128}; block_size in
  * {16, 32, 64}.  FP8 only: one scale per tensor (k_scale / v_scale, > 0 and
  * finite), or one per kv head as the page's KV-cache quantisation section
- * describes (§7.2 "为每个attention head单独计算scale"): k_scales / v_scales,
+ * describes (§7.2 "KV Cache量化", its first item): k_scales / v_scales,
  * optional device arrays of num_kv_heads positive finite floats (4-byte
  * aligned) that override the scalars when non-NULL.  Values in those arrays
  * are device data and are not checked. */

@@ -12,13 +12,13 @@
  *   - §6.2 "Paged Attention优化": attention for one head walks the
  *     sequence's block table, dot-products q with each key and accumulates a
  *     weighted sum of values; several sequences may point at the same prefix
- *     pages ("共享前缀优化").
+ *     pages (the section's list of optimisations).
  *   - §6.1 "Flash Attention实现": softmax kept with a running max and sum;
  *     the oracle uses the plain two-pass max-subtracted softmax, which the
  *     running form equals.
  *   - §7.2 "KV Cache量化": quantised KV is dequantised inside the attention
- *     ("零拷贝反量化"): value = e4m3(code) * scale, with one scale per tensor
- *     or, as the section describes, one scale per attention (kv) head.
+ *     kernel (its third item): value = e4m3(code) * scale, with one scale
+ *     per tensor or, as its first item has it, one per attention (kv) head.
  *   - §5.3 "分块上下文处理": a long prompt is processed in chunks; token i of
  *     a chunk of C tokens appended to a sequence of final length L sits at
  *     position L - C + i and attends to keys 0 .. L - C + i.

@@ -18,7 +18,7 @@ the pages of the sequences it checks.
 Shapes follow the in-flight-batching decode step of the TensorRT-LLM pages
 ("KV缓存管理细节", §4.2: paged KV, non-contiguous physical pages; §6.2 Paged
 Attention: block_tables [num_seqs, max_blocks]); prefix pages shared between
-sequences follow "共享前缀优化" (§6.2); chunked context follows §5.3.
+sequences follow the shared-prefix item of §6.2; chunked context follows §5.3.
 Pool layout: k_pool, v_pool = [num_blocks, num_kv_heads, block_size, head_dim].
 """
 from __future__ import annotations
