@@ -58,7 +58,8 @@ typedef enum pkv_status {
     PKV_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     PKV_ERR_DEVICE_BOUNDS = 5, /* a kernel met an out-of-range page id or slot */
-    PKV_ERR_DEVICE_TIMEOUT = 6 /* a bounded wait inside a kernel ran out */
+    PKV_ERR_DEVICE_TIMEOUT = 6, /* a bounded wait inside a kernel ran out */
+    PKV_ERR_OUT_OF_BLOCKS = 7   /* host page manager: the pool cannot supply the blocks */
 } pkv_status;
 
 typedef enum pkv_kv_dtype {
@@ -236,6 +237,110 @@ PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
 /* Text of the last CUDA error a call of this library met on the calling
  * thread (explains PKV_ERR_CUDA; "no error" if none).  Never NULL. */
 PKV_API const char *pkv_last_cuda_error(void);
+
+/* Copy whole blocks for copy-on-write of shared prefix pages (the page's
+ * §4.1 / §4.2: blocks are reused and shared between sequences; a shared
+ * block must be duplicated before one of its owners writes into it).
+ *   pairs        device, int32 [num_pairs][2]: (source block, destination
+ *                block), 4-byte aligned, as pkv_cache_append reports them.
+ *                Every destination must be distinct and must not be the
+ *                source of any pair in the same call (the manager's
+ *                destinations are freshly popped blocks, so this holds).
+ *   k_pool/v_pool as in pkv_kv_append; the whole block (all kv heads) of
+ *                both pools is copied.
+ * Asynchronous on `stream`; order it before the pkv_kv_append that writes
+ * into the destinations.  An out-of-range block id is skipped and recorded
+ * for pkv_get_device_error (PKV_ERR_DEVICE_BOUNDS). */
+PKV_API pkv_status pkv_copy_blocks(void *k_pool, void *v_pool, const pkv_pool_desc *pool,
+                                   const int32_t *pairs, int32_t num_pairs, void *stream);
+
+/* ---- Host KV-cache page manager ------------------------------------------
+ * The page "TensorRT-LLM框架解析与高性能推理优化实践", §4.1 (a KV-cache
+ * manager: paged cache, block reuse and prefix sharing, memory reclaim),
+ * §4.2 (KV缓存管理细节: blocks of one pool handed out and taken back, a block
+ * list per sequence that is its block table) and §5.2 (抢占策略实现:
+ * last-in-first-out preemption of running requests when the pool is short).
+ *
+ * Host memory only; no CUDA call.  A manager is not thread-safe: one caller
+ * at a time.  Its outputs are the device calls' inputs: slot mappings for
+ * pkv_kv_append, block pairs for pkv_copy_blocks, block tables and lengths
+ * for pkv_paged_attention / pkv_paged_prefill (copied to the device by the
+ * caller).  Sequence ids are caller-chosen non-negative int64 values.
+ *
+ * Policy, fixed so that results are reproducible:
+ *   - free blocks form a stack with block 0 on top at creation; allocation
+ *     pops the top, release pushes;
+ *   - a sequence forked from another shares the parent's first
+ *     ceil(num_tokens / block_size) blocks;
+ *   - a block with more than one owner is copied before a sequence writes
+ *     into it: a fresh block is popped and (old, new) reported;
+ *   - an append over several sequences is all-or-nothing;
+ *   - release pushes a sequence's blocks last page first; a block returns to
+ *     the free stack when its owner count reaches zero;
+ *   - preemption frees whole sequences, most recently admitted (added or
+ *     forked) first, skipping protected ones; nothing changes if that cannot
+ *     free enough.
+ * Errors: PKV_ERR_INVALID_ARG (null pointer, unknown or duplicate id, a
+ * count that would exceed max_blocks_per_seq, too small an output buffer)
+ * and PKV_ERR_OUT_OF_BLOCKS leave the manager unchanged. */
+typedef struct pkv_cache pkv_cache;
+
+/* Create a manager for a pool of num_blocks blocks of block_size tokens;
+ * tables have max_blocks_per_seq entries.  *out is owned by the caller and
+ * freed by pkv_cache_destroy. */
+PKV_API pkv_status pkv_cache_create(int32_t num_blocks, int32_t block_size,
+                                    int32_t max_blocks_per_seq, pkv_cache **out);
+PKV_API void pkv_cache_destroy(pkv_cache *cache);
+
+/* Free blocks / live sequences (-1 for a NULL manager). */
+PKV_API int32_t pkv_cache_num_free(const pkv_cache *cache);
+PKV_API int32_t pkv_cache_num_seqs(const pkv_cache *cache);
+/* Tokens held by a sequence, -1 if unknown. */
+PKV_API int32_t pkv_cache_length(const pkv_cache *cache, int64_t seq_id);
+
+/* Admit an empty sequence. */
+PKV_API pkv_status pkv_cache_add(pkv_cache *cache, int64_t seq_id);
+/* Admit `child` as the first num_tokens tokens of `parent` (0 <= num_tokens
+ * <= parent's length), sharing the blocks that hold them. */
+PKV_API pkv_status pkv_cache_fork(pkv_cache *cache, int64_t parent, int64_t child,
+                                  int32_t num_tokens);
+/* Give back a sequence's blocks and forget it. */
+PKV_API pkv_status pkv_cache_release(pkv_cache *cache, int64_t seq_id);
+
+/* Blocks (new pages plus copies) that pkv_cache_append of the same arguments
+ * would take; -1 if the request is invalid. */
+PKV_API int64_t pkv_cache_blocks_needed(pkv_cache *cache, const int64_t *seq_ids,
+                                        const int32_t *counts, int32_t n);
+
+/* Reserve slots for counts[i] new tokens of seq_ids[i] (distinct ids), in
+ * that order.  Writes the slots (block * block_size + offset) of the
+ * sum(counts) tokens, sequence after sequence, into slot_mapping
+ * (slot_capacity entries), and the copy-on-write pairs into copies
+ * (copy_capacity >= n pairs of int32: each sequence copies at most one
+ * block per call).  *num_slots and *num_copies receive the counts. */
+PKV_API pkv_status pkv_cache_append(pkv_cache *cache, const int64_t *seq_ids,
+                                    const int32_t *counts, int32_t n, int64_t *slot_mapping,
+                                    int64_t slot_capacity, int32_t *copies,
+                                    int32_t copy_capacity, int64_t *num_slots,
+                                    int32_t *num_copies);
+
+/* Release whole sequences, most recently admitted first and skipping the
+ * num_protected ids in protected_ids, until at least `needed` blocks are
+ * free.  The released ids go to victims (victim_capacity entries), in
+ * release order; *num_victims receives their count (0 if enough blocks were
+ * already free).  PKV_ERR_OUT_OF_BLOCKS if even releasing every unprotected
+ * sequence would not be enough. */
+PKV_API pkv_status pkv_cache_preempt_for(pkv_cache *cache, int32_t needed,
+                                         const int64_t *protected_ids, int32_t num_protected,
+                                         int64_t *victims, int32_t victim_capacity,
+                                         int32_t *num_victims);
+
+/* Block tables (int32 [n][max_blocks_per_seq], -1 past each sequence's last
+ * block) and context lengths (int32 [n]) of the listed sequences, in host
+ * memory, ready for one host-to-device copy. */
+PKV_API pkv_status pkv_cache_block_tables(const pkv_cache *cache, const int64_t *seq_ids,
+                                          int32_t n, int32_t *block_tables,
+                                          int32_t *context_lens);
 
 /* Static string for a status code (never NULL). */
 PKV_API const char *pkv_status_string(int32_t status);

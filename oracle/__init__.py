@@ -154,6 +154,17 @@ def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, kv_dtype="bf16",
 
 
 # ---- attention ---------------------------------------------------------------
+def copy_blocks(k_pool, v_pool, pairs) -> None:
+    """Copy-on-write of shared blocks, in place: for each (source, destination)
+    pair, the whole block (all kv heads) of both pools is duplicated.  The
+    page's §4.1 / §4.2 ("TensorRT-LLM框架解析与高性能推理优化实践"): blocks are
+    shared and reused, so a shared block is duplicated before an owner writes
+    into it."""
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        k_pool[dst] = k_pool[src]
+        v_pool[dst] = v_pool[src]
+
+
 def paged_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
                     kv_dtype="bf16", k_scale=1.0, v_scale=1.0, k_scales=None,
                     v_scales=None) -> np.ndarray:

@@ -12,6 +12,8 @@ Functions mirror the C entry points:
     paged_attention                 <- pkv_paged_attention
     paged_attention_noalloc         <- pkv_paged_attention_noalloc
     paged_prefill                   <- pkv_paged_prefill
+    copy_blocks                     <- pkv_copy_blocks
+    KVCacheManager                  <- pkv_cache_* (host page manager)
     get_device_error                <- pkv_get_device_error
     status_string                   <- pkv_status_string
 """
@@ -22,6 +24,7 @@ import os
 import threading
 from typing import Optional
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +33,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 PKV_OK = 0
 PKV_ERR_DEVICE_BOUNDS = 5
 PKV_ERR_DEVICE_TIMEOUT = 6
+PKV_ERR_OUT_OF_BLOCKS = 7
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
@@ -85,6 +89,32 @@ def lib():
             L.pkv_paged_prefill.restype = i32
             L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, i32,
                                             f32, vp, vp]
+            L.pkv_copy_blocks.restype = i32
+            L.pkv_copy_blocks.argtypes = [vp, vp, pd, vp, i32, vp]
+            L.pkv_cache_create.restype = i32
+            L.pkv_cache_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
+            L.pkv_cache_destroy.restype = None
+            L.pkv_cache_destroy.argtypes = [vp]
+            for name in ("pkv_cache_num_free", "pkv_cache_num_seqs"):
+                getattr(L, name).restype = i32
+                getattr(L, name).argtypes = [vp]
+            L.pkv_cache_length.restype = i32
+            L.pkv_cache_length.argtypes = [vp, i64]
+            L.pkv_cache_add.restype = i32
+            L.pkv_cache_add.argtypes = [vp, i64]
+            L.pkv_cache_fork.restype = i32
+            L.pkv_cache_fork.argtypes = [vp, i64, i64, i32]
+            L.pkv_cache_release.restype = i32
+            L.pkv_cache_release.argtypes = [vp, i64]
+            L.pkv_cache_blocks_needed.restype = i64
+            L.pkv_cache_blocks_needed.argtypes = [vp, vp, vp, i32]
+            L.pkv_cache_append.restype = i32
+            L.pkv_cache_append.argtypes = [vp, vp, vp, i32, vp, i64, vp, i32,
+                                           ctypes.POINTER(i64), ctypes.POINTER(i32)]
+            L.pkv_cache_preempt_for.restype = i32
+            L.pkv_cache_preempt_for.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.POINTER(i32)]
+            L.pkv_cache_block_tables.restype = i32
+            L.pkv_cache_block_tables.argtypes = [vp, vp, i32, vp, vp]
             L.pkv_get_device_error.restype = i32
             L.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
             L.pkv_last_cuda_error.restype = ctypes.c_char_p
@@ -264,6 +294,114 @@ def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens, m
                                    _stream(stream)),
            "pkv_paged_prefill")
     return out
+
+
+def copy_blocks(k_pool, v_pool, pairs, stream=None, k_scale=1.0, v_scale=1.0) -> None:
+    """Copy whole blocks of both pools: pairs is an int32 CUDA tensor [n, 2]
+    of (source, destination) block ids, as KVCacheManager.append reports."""
+    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n, 2]")
+    desc = pool_desc(k_pool, k_scale, v_scale)
+    if v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("k_pool and v_pool differ")
+    n = int(pairs.shape[0])
+    if n == 0:
+        return
+    _check(lib().pkv_copy_blocks(_ptr(k_pool), _ptr(v_pool), ctypes.byref(desc), _ptr(pairs),
+                                 n, _stream(stream)), "pkv_copy_blocks")
+
+
+def _np_ptr(a: np.ndarray) -> ctypes.c_void_p:
+    return ctypes.c_void_p(a.ctypes.data) if a.size else ctypes.c_void_p(0)
+
+
+class KVCacheManager:
+    """Host page manager of a paged KV pool (pkv_cache_* in the C library).
+
+    Produces, in host numpy arrays, the device calls' inputs: slot mappings,
+    copy-on-write block pairs, block tables and context lengths."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        h = ctypes.c_void_p(0)
+        _check(lib().pkv_cache_create(int(num_blocks), int(block_size),
+                                      int(max_blocks_per_seq), ctypes.byref(h)),
+               "pkv_cache_create")
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            lib().pkv_cache_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may be gone already
+            pass
+
+    def num_free(self) -> int:
+        return int(lib().pkv_cache_num_free(self._h))
+
+    def num_seqs(self) -> int:
+        return int(lib().pkv_cache_num_seqs(self._h))
+
+    def length(self, seq_id: int) -> int:
+        return int(lib().pkv_cache_length(self._h, int(seq_id)))
+
+    def add(self, seq_id: int) -> int:
+        return int(lib().pkv_cache_add(self._h, int(seq_id)))
+
+    def fork(self, parent: int, child: int, num_tokens: int) -> int:
+        return int(lib().pkv_cache_fork(self._h, int(parent), int(child), int(num_tokens)))
+
+    def release(self, seq_id: int) -> int:
+        return int(lib().pkv_cache_release(self._h, int(seq_id)))
+
+    @staticmethod
+    def _ids_counts(seq_ids, counts):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        if ids.shape != cnt.shape or ids.ndim != 1:
+            raise ValueError("seq_ids and counts must be 1-D and of equal length")
+        return ids, cnt
+
+    def blocks_needed(self, seq_ids, counts) -> int:
+        ids, cnt = self._ids_counts(seq_ids, counts)
+        return int(lib().pkv_cache_blocks_needed(self._h, _np_ptr(ids), _np_ptr(cnt), len(ids)))
+
+    def append(self, seq_ids, counts):
+        """(status, slot_mapping int64 [sum counts], copies int32 [k, 2])."""
+        ids, cnt = self._ids_counts(seq_ids, counts)
+        n = len(ids)
+        slots = np.empty(max(int(cnt[cnt > 0].sum()), 0), np.int64)
+        copies = np.empty((max(n, 1), 2), np.int32)
+        ns, nc = ctypes.c_int64(0), ctypes.c_int32(0)
+        st = lib().pkv_cache_append(self._h, _np_ptr(ids), _np_ptr(cnt), n, _np_ptr(slots),
+                                    slots.size, _np_ptr(copies), n, ctypes.byref(ns),
+                                    ctypes.byref(nc))
+        return int(st), slots[:ns.value].copy(), copies[:nc.value].copy()
+
+    def preempt_for(self, needed: int, protected=()):
+        """(status, list of released sequence ids, in release order)."""
+        prot = np.ascontiguousarray(list(protected), dtype=np.int64)
+        cap = max(self.num_seqs(), 1)
+        victims = np.empty(cap, np.int64)
+        nv = ctypes.c_int32(0)
+        st = lib().pkv_cache_preempt_for(self._h, int(needed), _np_ptr(prot), len(prot),
+                                         _np_ptr(victims), cap, ctypes.byref(nv))
+        return int(st), [int(v) for v in victims[:nv.value]]
+
+    def block_tables(self, seq_ids):
+        """(int32 [n, max_blocks_per_seq] tables, int32 [n] context lengths)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = len(ids)
+        tab = np.empty((n, self.max_blocks_per_seq), np.int32)
+        lens = np.empty(n, np.int32)
+        _check(lib().pkv_cache_block_tables(self._h, _np_ptr(ids), n, _np_ptr(tab),
+                                            _np_ptr(lens)), "pkv_cache_block_tables")
+        return tab, lens
 
 
 def get_device_error(stream=None) -> int:

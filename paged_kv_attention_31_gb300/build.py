@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "decode_mma.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "decode_mma.cu", "prefill.cu", "noalloc.cu",
+           "kv_cache_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -52,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
             jobs.append([nvcc(), *_flags(extra_flags), "-c", s, "-o", o])

@@ -515,9 +515,9 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     }
   }
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + size_t(gw) * D + lane * DV;
-#pragma unroll
   const int kvh = (gw - s * p.num_q_heads) / (p.num_q_heads / p.num_kv_heads);
   const float vm = p.v_scales ? p.v_mult * __ldg(p.v_scales + kvh) : p.v_mult;
+#pragma unroll
   for (int e = 0; e < DV; ++e) dst[e] = __float2bfloat16_rn(lsum > 0.f ? a[e] / lsum * vm : 0.f);
 }
 

@@ -114,6 +114,7 @@ const char* pkv_status_string(int32_t s) {
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_DEVICE_BOUNDS: return "device data out of range (page id, slot or length)";
     case PKV_ERR_DEVICE_TIMEOUT: return "bounded wait in a kernel ran out";
+    case PKV_ERR_OUT_OF_BLOCKS: return "not enough free KV-cache blocks";
     default: return "unknown status";
   }
 }
@@ -150,6 +151,29 @@ pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* sl
   p.fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
   p.err = dev->err;
   return from_cuda(pkv::launch_kv_append(p, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const pkv_pool_desc* pool,
+                           const int32_t* pairs, int32_t num_pairs, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_pairs < 0) return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !pairs || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 3))
+    return PKV_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  pkv::CopyParams p;
+  p.pairs = pairs;
+  p.num_pairs = num_pairs;
+  p.num_blocks = pool->num_blocks;
+  p.block_bytes = int64_t(pool->num_kv_heads) * pool->block_size * pool->head_dim *
+                  (pool->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2);
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.err = dev->err;
+  return from_cuda(pkv::launch_copy_blocks(p, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,

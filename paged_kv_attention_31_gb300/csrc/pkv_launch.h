@@ -85,6 +85,18 @@ inline DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, in
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+
+// Whole-block copies (all kv heads of K and of V) for copy-on-write.
+struct CopyParams {
+  const int32_t* pairs;   // [num_pairs][2]: (source block, destination block)
+  int32_t num_pairs;
+  int32_t num_blocks;
+  int64_t block_bytes;    // Hkv * P * D * element size: one block of one pool
+  void* k_pool;
+  void* v_pool;
+  int32_t* err;
+};
+cudaError_t launch_copy_blocks(const CopyParams& p, int num_sms, cudaStream_t stream);
 // split planner and partial merge of the decode (decode.cu)
 void launch_decode_plan(const DecodeParams& p, cudaStream_t stream);
 void launch_decode_merge(const DecodeParams& p, cudaStream_t stream);

@@ -28,7 +28,9 @@ def lib():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("pkv_kv_append", "pkv_paged_attention", "pkv_paged_attention_workspace_size",
-              "pkv_paged_prefill", "pkv_get_device_error", "pkv_status_string", "pkv_version"):
+              "pkv_paged_prefill", "pkv_get_device_error", "pkv_status_string", "pkv_version",
+              "pkv_copy_blocks", "pkv_cache_create", "pkv_cache_append", "pkv_cache_fork",
+              "pkv_cache_preempt_for", "pkv_cache_block_tables"):
         assert n in names
 
 
@@ -44,7 +46,7 @@ def test_internal_symbols_hidden(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert pkv.status_string(s)
     assert pkv.status_string(99) == "unknown status"
 
@@ -91,6 +93,18 @@ def test_argument_validation_before_any_cuda_call(lib):
     d64 = _desc(head_dim=64)
     assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d64), one, 4, one, 1, 4, 16, 16,
                                  0.1, one, z) == 2
+
+
+def test_copy_blocks_validation_before_any_cuda_call(lib):
+    d = _desc()
+    z = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    assert lib.pkv_copy_blocks(one, one, ctypes.byref(d), one, 0, z) == 0      # no-op
+    assert lib.pkv_copy_blocks(one, one, ctypes.byref(d), one, -1, z) == 1
+    assert lib.pkv_copy_blocks(z, one, ctypes.byref(d), one, 2, z) == 1        # null pool
+    assert lib.pkv_copy_blocks(one, one, ctypes.byref(d), z, 2, z) == 1        # null pairs
+    assert lib.pkv_copy_blocks(one, ctypes.c_void_p(264), ctypes.byref(d), one, 2, z) == 1
+    assert lib.pkv_copy_blocks(one, one, ctypes.byref(d), ctypes.c_void_p(258), 2, z) == 1
 
 
 def test_workspace_size_is_positive(lib):
