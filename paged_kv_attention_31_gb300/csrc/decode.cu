@@ -189,6 +189,8 @@ __global__ void __launch_bounds__(512) decode_plan_kernel(const DecodeParams p) 
   __shared__ int hist[kMaxBuckets];
   __shared__ int offs[kMaxBuckets];
   const int nb = p.partition / kTT + 1;  // bucket = tiles in the item (0 .. partition/TT)
+  pdl_launch_dependents();
+  pdl_wait();  // the step's kv_append (and anything before it) is done
   for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
@@ -247,6 +249,7 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
     for (int s = 0; s < ST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
+  pdl_wait();  // planner output and this step's appends are visible
   if (threadIdx.x == 0) {
     misc[0] = atomicAdd(p.counters + 1, 1);
     misc[2] = 0;
@@ -484,12 +487,14 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
     __syncthreads();  // shared state is reused by the next unit
     unit = next_unit;
   }
+  pdl_launch_dependents();  // out of work: the merge may launch
 }
 
 // ---- merge -------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
   constexpr int DV = D / 32;
+  pdl_wait();  // every partial of the decode grid is written
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= p.num_seqs * p.num_q_heads) return;
@@ -554,12 +559,15 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) 
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NTHR, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  decode_plan_kernel<<<1, 512, 0, stream>>>(p);
-  const int grid = num_sms * per_sm;
-  kern<<<grid, C::NTHR, smem, stream>>>(p);
+  if ((e = launch_pdl(decode_plan_kernel, dim3(1), dim3(512), 0, stream, p)) != cudaSuccess)
+    return e;
+  if ((e = launch_pdl(kern, dim3(num_sms * per_sm), dim3(C::NTHR), smem, stream, p)) !=
+      cudaSuccess)
+    return e;
   if (p.max_splits > 1) {
     const int warps = p.num_seqs * p.num_q_heads;
-    decode_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p);
+    e = launch_pdl(decode_merge_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, stream, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -577,16 +585,15 @@ cudaError_t launch_g(const DecodeParams& p, int num_sms, cudaStream_t stream) {
 
 }  // namespace
 
-void launch_decode_plan(const DecodeParams& p, cudaStream_t stream) {
-  decode_plan_kernel<<<1, 512, 0, stream>>>(p);
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t stream) {
+  return launch_pdl(decode_plan_kernel, dim3(1), dim3(512), 0, stream, p);
 }
 
-void launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
   const int warps = p.num_seqs * p.num_q_heads;
-  if (p.head_dim == 128)
-    decode_merge_kernel<128><<<(warps + 7) / 8, 256, 0, stream>>>(p);
-  else
-    decode_merge_kernel<64><<<(warps + 7) / 8, 256, 0, stream>>>(p);
+  const dim3 grid((warps + 7) / 8), block(256);
+  return p.head_dim == 128 ? launch_pdl(decode_merge_kernel<128>, grid, block, 0, stream, p)
+                           : launch_pdl(decode_merge_kernel<64>, grid, block, 0, stream, p);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream) {

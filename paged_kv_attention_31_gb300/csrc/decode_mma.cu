@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kNW * 32)
     for (int s = 0; s < kST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
+  pdl_wait();  // planner output and this step's appends are visible
   if (threadIdx.x == 0) {
     misc[0] = atomicAdd(p.counters + 1, 1);
     misc[2] = 0;
@@ -471,6 +472,7 @@ __global__ void __launch_bounds__(kNW * 32)
     __syncthreads();           // shared state is reused by the next unit
     unit = next_unit;
   }
+  pdl_launch_dependents();  // out of work: the merge may launch
 }
 
 template <int G, bool FP8>
@@ -495,9 +497,10 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  launch_decode_plan(p, stream);
-  kern<<<num_sms * per_sm, kNW * 32, smem, stream>>>(tk, tv, p);
-  if (p.max_splits > 1) launch_decode_merge(p, stream);
+  if ((e = launch_decode_plan(p, stream)) != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(num_sms * per_sm), dim3(kNW * 32), smem, stream, tk, tv, p);
+  if (e != cudaSuccess) return e;
+  if (p.max_splits > 1 && (e = launch_decode_merge(p, stream)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@ __device__ __forceinline__ void store_row_chunk<true>(uint8_t* pool, int64_t ele
 
 template <bool FP8>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  pdl_launch_dependents();  // the next kernel may start its prologue now
   const int chunks = p.head_dim / 8;  // 16-byte chunks per (token, head) row
   const int64_t per_tok = int64_t(p.num_kv_heads) * chunks;
   const int64_t total = int64_t(p.num_tokens) * per_tok;

@@ -29,6 +29,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+// A kernel launched with the programmatic stream-serialization attribute may
+// begin while the kernel before it in the stream is still running.  It calls
+// pdl_wait() before it reads or writes any global memory that an earlier
+// kernel of the stream touches: the wait returns once those kernels have
+// completed and their writes are visible.  pdl_launch_dependents() lets the
+// next kernel of the stream start early (its own pdl_wait() still orders its
+// memory accesses after this grid).  Both are no-ops for a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

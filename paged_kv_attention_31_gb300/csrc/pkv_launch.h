@@ -6,7 +6,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes (it must call pdl_wait() before
+// touching memory that kernel uses), hiding launch latency between the
+// kernels of one step.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct AppendParams {
   const void* k_new;            // bf16 [T][Hkv][D]
@@ -98,8 +120,8 @@ struct CopyParams {
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, int num_sms, cudaStream_t stream);
 // split planner and partial merge of the decode (decode.cu)
-void launch_decode_plan(const DecodeParams& p, cudaStream_t stream);
-void launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
 // head_dim 128, 4 or 8 q heads per kv head, bf16 or FP8 KV (decode_mma.cu)
 cudaError_t launch_decode_mma(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);
 // Returns cudaErrorNotSupported for shapes without a kernel instance.

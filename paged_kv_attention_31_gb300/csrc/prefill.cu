@@ -182,6 +182,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  pdl_wait();  // inputs written by earlier kernels of the stream are visible
   // heavier (later, longer-context) tile pairs are launched first
   const int pair = int(gridDim.x) - 1 - int(blockIdx.x);
   const int h = blockIdx.y, s = blockIdx.z;
@@ -576,7 +577,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
   // one CTA per pair of 128-row query tiles
   dim3 grid((p.tiles_per_seq + kTiles - 1) / kTiles, p.num_kv_heads, p.num_seqs);
   if (grid.z > 65535) return cudaErrorInvalidValue;
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  e = launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
