@@ -309,11 +309,13 @@ def run_gpu(args):
         max_q = int(w.prefill_chunk_lens.max())
     stream = torch.cuda.current_stream(dev)
 
-    def step(q, k_new, v_new, slots, bt, cl, ev=None):
+    def step(q, k_new, v_new, slots, bt, cl, qp=None, cu=None, pbt=None, pcl=None, ev=None,
+             o=None, op=None):
+        o = out if o is None else o
         pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
         if ev is not None:
             ev[0].record(stream)
-        pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=out,
+        pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
                             workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
                             partition_tokens=args.partition)
         if ev is not None:
@@ -321,13 +323,15 @@ def run_gpu(args):
         if has_prefill:
             if ev is not None:
                 ev[2].record(stream)
-            pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp,
-                              d["prefill_block_tables"], d["prefill_context_lens"], max_q,
-                              w.scale, out=out_p)
+            pkv.paged_prefill(qp, cu, kp, vp, pbt, pcl, max_q, w.scale,
+                              out=out_p if op is None else op)
             if ev is not None:
                 ev[3].record(stream)
 
     args_dev = (d["q"], d["k_new"], d["v_new"], d["slots"], d["block_tables"], d["context_lens"])
+    if has_prefill:
+        args_dev += (d["q_prefill"], d["cu_seqlens_q"], d["prefill_block_tables"],
+                     d["prefill_context_lens"])
     for _ in range(args.warmup):
         step(*args_dev)
     torch.cuda.synchronize(dev)
@@ -382,28 +386,59 @@ def run_gpu(args):
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # --- end to end through the public API from pinned host memory ------------------
+    # Every step copies its inputs from pinned host memory and its outputs
+    # back.  Copies run on their own streams into double-buffered device
+    # inputs and outputs, so step i's copies overlap the kernels of step i - 1
+    # (the kernels themselves stay in order on the compute stream: each
+    # step's appends precede its attention).
     host = [x.cpu().pin_memory() for x in args_dev]
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dev_bufs = [torch.empty_like(x) for x in args_dev]
+    outs_dev = [out] + ([out_p] if has_prefill else [])
+    nbuf = 2
+    sets = [[torch.empty_like(x) for x in args_dev] for _ in range(nbuf)]
+    osets = [[torch.empty_like(x) for x in outs_dev] for _ in range(nbuf)]
+    ohost = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs_dev]
+             for _ in range(nbuf)]
     h2d = sum(x.numel() * x.element_size() for x in host)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = sum(x.numel() * x.element_size() for x in outs_dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]      # inputs of set b landed
+    ev_done = [torch.cuda.Event() for _ in range(nbuf)]    # kernels done with set b
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]     # outputs of set b copied back
 
-    def e2e_step():
-        for hb, db in zip(host, dev_bufs):
-            db.copy_(hb, non_blocking=True)
-        step(*dev_bufs)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % nbuf
+        if i >= nbuf:
+            h2d_s.wait_event(ev_done[b])
+        with torch.cuda.stream(h2d_s):
+            for hb, db in zip(host, sets[b]):
+                db.copy_(hb, non_blocking=True)
+        ev_in[b].record(h2d_s)
+        stream.wait_event(ev_in[b])
+        if i >= nbuf:
+            stream.wait_event(ev_out[b])
+        step(*sets[b], o=osets[b][0], op=osets[b][1] if has_prefill else None)
+        ev_done[b].record(stream)
+        d2h_s.wait_event(ev_done[b])
+        with torch.cuda.stream(d2h_s):
+            for hb, db in zip(ohost[b], osets[b]):
+                hb.copy_(db, non_blocking=True)
+        ev_out[b].record(d2h_s)
 
-    for _ in range(min(args.warmup, 3)):
-        e2e_step()
+    for i in range(min(args.warmup, 3)):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    h2d_s.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    for b in range(nbuf):
+        stream.wait_event(ev_out[b])
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    if not torch.equal(ohost[(args.steps - 1) % nbuf][0], out.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
     e2e_ms = e0.elapsed_time(e1) / args.steps
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error during the timed region")

@@ -71,10 +71,13 @@ constexpr int kOffBar = kOffP + 2 * kTiles * kPBytes;  // P double-buffered per 
 // barriers: q, k[3], v[3], kfree[3], vfree[3], s[2][2], p[2][2], o[2][2]
 constexpr int kNumBars = 1 + 4 * kStages + 6 * kTiles;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
+// CTA order: end positions of up to kMaxRankGroups (sequence, tile pair) groups
+constexpr int kMaxRankGroups = 256;
+constexpr int kOffRank = kOffMisc + 16;
 // The 128-byte-swizzled tiles need a 1024-aligned base; dynamic shared memory
 // starts at least 128-aligned, so at most 896 bytes of padding are needed.
 constexpr int kMaxPad = 1024 - 128;
-constexpr int kSmemBytes = kOffMisc + 16 + kMaxPad;
+constexpr int kSmemBytes = kOffRank + 4 * kMaxRankGroups + kMaxPad;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------------
@@ -183,11 +186,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   pdl_wait();  // inputs written by earlier kernels of the stream are visible
-  // heavier (later, longer-context) tile pairs are launched first
-  const int pair = int(gridDim.x) - 1 - int(blockIdx.x);
-  const int h = blockIdx.y, s = blockIdx.z;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > uint32_t(kMaxPad)) {  // cannot happen with a 128-aligned base; never index past the end
+    if (threadIdx.x == 0) record_error(p.err, kDevBadPage);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   const int G = p.num_q_heads / p.num_kv_heads;
   const int TQ = kM / G;
+
+  // Longest work first: CTA k takes kv head k % Hkv of the (sequence, tile
+  // pair) group of rank k / Hkv, ranked by the position of the group's last
+  // query (its key count), ties by group index.  The block scheduler starts
+  // CTAs in index order, so this is the longest-processing-time-first list
+  // schedule; groups past a sequence's chunk rank last and exit at once.
+  const int max_pairs = (p.tiles_per_seq + kTiles - 1) / kTiles;
+  const int n_groups = p.num_seqs * max_pairs;
+  const int h = int(blockIdx.x) % p.num_kv_heads;
+  int group = int(blockIdx.x) / p.num_kv_heads;
+  if (n_groups > kMaxRankGroups) {  // too many to rank here: later tile pairs first
+    group = (group / max_pairs) * max_pairs + (max_pairs - 1 - group % max_pairs);
+  } else {
+    int* const gend = reinterpret_cast<int*>(smem + kOffRank);
+    int* const gsel = reinterpret_cast<int*>(smem + kOffMisc + 8);
+    for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
+      const int gs = g / max_pairs, ta = (g - gs * max_pairs) * kTiles * TQ;
+      const int c0 = __ldg(p.cu_seqlens_q + gs), cg = __ldg(p.cu_seqlens_q + gs + 1) - c0;
+      gend[g] = (cg > 0 && ta < cg) ? max(0, __ldg(p.context_lens + gs) - cg + min(cg, ta + kTiles * TQ))
+                                    : -1;
+    }
+    __syncthreads();
+    const int want = group;
+    for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
+      const int e = gend[g];
+      int r = 0;
+      for (int o = 0; o < n_groups; ++o) {
+        const int eo = gend[o];
+        r += (eo > e || (eo == e && o < g)) ? 1 : 0;
+      }
+      if (r == want) *gsel = g;
+    }
+    __syncthreads();
+    group = *gsel;
+    __syncthreads();  // the rank area is reused below only through other offsets
+  }
+  const int s = group / max_pairs, pair = group - s * max_pairs;
   const int q0 = __ldg(p.cu_seqlens_q + s);
   const int C = __ldg(p.cu_seqlens_q + s + 1) - q0;
   const int tokA = pair * kTiles * TQ;            // first chunk token of tile 0
@@ -198,14 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) record_error(p.err, kDevBadPage);
     return;
   }
-
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  if (pad > uint32_t(kMaxPad)) {  // cannot happen with a 128-aligned base; never index past the end
-    if (threadIdx.x == 0) record_error(p.err, kDevBadPage);
-    return;
-  }
-  uint8_t* smem = smem_raw + pad;
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
@@ -574,9 +610,11 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  // one CTA per pair of 128-row query tiles
-  dim3 grid((p.tiles_per_seq + kTiles - 1) / kTiles, p.num_kv_heads, p.num_seqs);
-  if (grid.z > 65535) return cudaErrorInvalidValue;
+  // one CTA per pair of 128-row query tiles of one kv head
+  const int64_t ctas =
+      int64_t((p.tiles_per_seq + kTiles - 1) / kTiles) * p.num_kv_heads * p.num_seqs;
+  if (ctas > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+  const dim3 grid{static_cast<unsigned>(ctas)};
   e = launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -59,6 +59,25 @@ def test_groups_blocks_and_ragged_chunks(G, P):
     _check(w, out)
 
 
+@pytest.mark.parametrize("n_chunks", [24, 40])
+def test_many_chunks_cta_order(n_chunks):
+    # The kernel ranks (sequence, tile pair) groups longest first when there
+    # are at most 256 of them (24 chunks x up to 10 pairs) and falls back to a
+    # fixed order above that (40 chunks): both must give the same results.
+    rng = np.random.default_rng(77 + n_chunks)
+    priors = [int(x) for x in rng.integers(0, 600, n_chunks)]
+    chunks = [int(x) for x in rng.integers(1, 321, n_chunks)]
+    chunks[0] = 320                                   # max_q_len 320: 10 pairs at G = 8
+    w = W.make_mixed(f"prefill_many_{n_chunks}", 4242 + n_chunks, [16], priors, chunks, 8, 1,
+                     128, 16)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check(w, out, seqs=sorted({0, 1, n_chunks // 2, n_chunks - 1,
+                                int(np.argmax(w.prefill_context_lens))}))
+
+
 def test_never_written_slots_past_the_end_do_not_leak():
     # fill everything past each sequence's last token with NaN bit patterns
     w = W.make_mixed("prefill_nan_tail", 1234, [30], [5, 70], [50, 27], 32, 8, 128, 32)
