@@ -4,8 +4,8 @@
 // "TensorRT-LLM框架解析与高性能推理优化实践" §5.3 (分块上下文处理): a long prompt
 // is processed as chunks interleaved with decode steps; each chunk's queries
 // attend causally to everything before them in the sequence, whose K/V sit
-// in pages (§4.2, §6.2).  §6.1 (Flash Attention实现): 64-128-token key tiles,
-// double buffering, running max / sum, partial results kept on chip.
+// in pages (§4.2, §6.2).  §6.1 (Flash Attention实现): key tiles, double
+// buffering, running max / sum, partial results kept on chip.
 //
 // A query tile is 128 rows: TQ = 128/G chunk tokens x the G q heads that
 // share one kv head (row r = token r / G, head r % G), so every K/V page is
@@ -13,28 +13,29 @@
 // (one per SM) takes two consecutive tiles of one (sequence, kv head) and
 // specialises its warps:
 //   warps 9, 10 loaders: TMA of Q and the K pages (warp 9) and of the V
-//               pages (warp 10) into 3-stage rings of 64-key blocks shared by
-//               both tiles; page ids from the block table, read a few
+//               pages (warp 10) into 2-stage rings of 128-key blocks shared
+//               by both tiles; page ids from the block table, read a few
 //               blocks ahead; pages past the sequence use an out-of-range
-//               coordinate so TMA fills zeros.  Keeping loads out of the MMA
-//               warp keeps their latencies off the tensor core's issue path.
+//               coordinate so TMA fills zeros.
 //   warp 8      every tcgen05.mma (one elected lane):
-//                 S_t = Q_t K_j^T  (M=128, N=64, K=128 -> TMEM, fp32)
-//                 O_t += P_t V_j   (M=128, N=128, K=64 -> TMEM, fp32)
+//                 S_t = Q_t K_j^T  (M=128, N=128, K=128; A, B in shared memory)
+//                 O_t += P_t V_j   (M=128, N=128, K=128; A = P in TMEM, B = V)
 //   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: one thread
-//   warps 4-7   per row (TMEM lane): tcgen05.ld of S, causal mask, running
-//               max kept with a lag of up to 2^8 (O is rescaled in TMEM only
-//               when the max grows by more; the final normalisation uses the
-//               same max, so the result is exact), P = 2^(s - m) rounded to
-//               bf16 into 128-byte-swizzled shared memory.
-// Hand-offs are mbarriers only: tcgen05.commit signals "S ready", "O
-// updated" and "K / V stage free"; the softmax warps signal "P ready".  S is
-// double-buffered per tile in TMEM and issued two key blocks ahead, so the
-// next scores are ready when a softmax warpgroup finishes a block; while one
-// tile's softmax runs, the tensor core works on the other tile.  P is
-// double-buffered per tile too, so a warpgroup writes block j + 1's P while
-// the PV of block j still runs; only a rescale of O waits for the latest PV.
-// K and V have separate 3-stage rings (K is needed two blocks before V).
+//   warps 4-7   per row (TMEM lane).  A first pass over S (tcgen05.ld) takes
+//               the block max with the causal mask; the running max moves
+//               only when it grows by more than 2^8 (O is then rescaled in
+//               TMEM; the final normalisation uses the same max, so the
+//               result is exact); a second pass writes P = 2^(s - m) as bf16
+//               pairs over the first half of S's own TMEM columns.
+// TMEM (512 columns): S_t at 128 t, O_t at 256 + 128 t.  P never leaves
+// TMEM: the PV product reads its A operand there, so shared memory holds
+// only Q, K and V and feeds one operand per PV MMA.  Per tile the chain is
+// S_j -> softmax_j -> (PV_j, S_{j+1}); the MMA warp alternates the tiles, so
+// while one tile's softmax runs the tensor core works on the other tile.
+// Every hand-off is an mbarrier: tcgen05.commit signals "S ready", "last PV
+// done" and "K / V stage free"; the softmax warps signal "P ready".  The
+// commit behind "S_{j+1} ready" also covers PV_j, so the softmax of block
+// j + 1 may rescale O without another wait.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,29 +48,28 @@ namespace {
 
 constexpr int kD = 128;          // head_dim
 constexpr int kM = 128;          // query rows per tile
-constexpr int kNK = 64;          // keys per block
+constexpr int kNK = 128;         // keys per block
 constexpr int kTiles = 2;        // query tiles per CTA
-constexpr int kStages = 3;       // K/V ring depth (key blocks)
+constexpr int kStagesK = 2;      // K ring depth (key blocks)
+constexpr int kStagesV = 2;      // V ring depth (key blocks)
 constexpr int kSoftmaxThreads = 128 * kTiles;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;   // warp 8: issues every tcgen05.mma
 constexpr int kKLoadWarp = kMmaWarp + 1;         // warp 9: TMA of Q and of the K ring
 constexpr int kVLoadWarp = kMmaWarp + 2;         // warp 10: TMA of the V ring
 constexpr int kThreads = kSoftmaxThreads + 3 * 32;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S of tile t, buffer b at 64 (2 t + b); O of tile t at 256 + 128 t
+// TMEM columns: S (then P) of tile t at 128 t, O of tile t at 256 + 128 t
 constexpr uint32_t kColS = 0, kColO = 256;
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kQBytes = 2 * kM * 128;        // 32 KB per tile: two d-halves of [128 rows][128 B]
-constexpr int kKVStageBytes = 2 * kNK * 128; // 16 KB: two d-halves of [64 keys][128 B]
-constexpr int kPBytes = kM * 128;            // 16 KB per tile and buffer: [128 rows][64 keys bf16]
+constexpr int kKVStageBytes = 2 * kNK * 128; // 32 KB: two d-halves of [128 keys][128 B]
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTiles * kQBytes;
-constexpr int kOffV = kOffK + kStages * kKVStageBytes;
-constexpr int kOffP = kOffV + kStages * kKVStageBytes;
-constexpr int kOffBar = kOffP + 2 * kTiles * kPBytes;  // P double-buffered per tile
-// barriers: q, k[3], v[3], kfree[3], vfree[3], s[2][2], p[2][2], o[2][2]
-constexpr int kNumBars = 1 + 4 * kStages + 6 * kTiles;
+constexpr int kOffV = kOffK + kStagesK * kKVStageBytes;
+constexpr int kOffBar = kOffV + kStagesV * kKVStageBytes;
+// barriers: q, k[SK], kfree[SK], v[SV], vfree[SV], s[tiles], p[tiles], o[tiles]
+constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 // CTA order: end positions of up to kMaxRankGroups (sequence, tile pair) groups
 constexpr int kMaxRankGroups = 256;
@@ -117,22 +117,36 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
+// 32 consecutive fp32 columns of this thread's TMEM lane (load and wait).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 64 consecutive fp32 columns of this thread's TMEM lane (one load, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   uint32_t r[32];
@@ -161,6 +175,39 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// max(a, b, c) in one instruction (3-input max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is 128 lanes x K with two bf16 per
+// 32-bit column (K-major), one elected thread.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane; completion is
+// awaited separately with tmem_wait_st().
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format:
 // start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
 // offset >> 4 in 32-45, version 1 in 46-47, swizzle mode 2 = 128B in 61-63).
@@ -180,7 +227,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// The register file is handed out per group of four warps, so the 9-warp
+// The register file is handed out per group of four warps, so the 11-warp
 // CTA is budgeted as 12 warps: at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -245,18 +292,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  uint8_t* sP = smem + kOffP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_q = bar;
-  uint64_t* bar_k = bar + 1;                      // [kStages] K block landed
-  uint64_t* bar_v = bar_k + kStages;              // [kStages] V block landed
-  uint64_t* bar_kfree = bar_v + kStages;          // [kStages] S MMAs done with the K stage
-  uint64_t* bar_vfree = bar_kfree + kStages;      // [kStages] PV MMAs done with the V stage
-  // per tile t and buffer b = block & 1 (one barrier per buffer, so a side
-  // that runs a block ahead never aliases a phase):
-  uint64_t* bar_s = bar_vfree + kStages;          // [kTiles][2] S_t buffer ready
-  uint64_t* bar_p = bar_s + 2 * kTiles;           // [kTiles][2] P_t buffer written (4 warps)
-  uint64_t* bar_o = bar_p + 2 * kTiles;           // [kTiles][2] PV from that P buffer done
+  uint64_t* bar_k = bar + 1;                      // [kStagesK] K block landed
+  uint64_t* bar_kfree = bar_k + kStagesK;         // [kStagesK] S MMAs done with the K stage
+  uint64_t* bar_v = bar_kfree + kStagesK;         // [kStagesV] V block landed
+  uint64_t* bar_vfree = bar_v + kStagesV;         // [kStagesV] PV MMAs done with the V stage
+  // per tile, one phase per key block (each side waits every phase in order)
+  uint64_t* bar_s = bar_vfree + kStagesV;         // [kTiles] S_t of the next block ready
+  uint64_t* bar_p = bar_s + kTiles;               // [kTiles] P_t written (4 warps)
+  uint64_t* bar_o = bar_p + kTiles;               // [kTiles] last PV of tile t done (one phase)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -269,22 +314,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb1 = ntok1 > 0 ? (L - C + tokA + TQ + ntok1 - 1) / kNK + 1 : 0;
   const int nblk = max(nb0, nb1);                 // key blocks loaded for the CTA
   const int npages = (L + P - 1) / P;
-  const int pages_per_blk = kNK / P;
+  const int pages_per_blk = kNK / P;              // 2 .. 8
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesK; ++i) {
       mbar_init(&bar_k[i], 1);
-      mbar_init(&bar_v[i], 1);
       mbar_init(&bar_kfree[i], 1);
+    }
+    for (int i = 0; i < kStagesV; ++i) {
+      mbar_init(&bar_v[i], 1);
       mbar_init(&bar_vfree[i], 1);
     }
     for (int t = 0; t < kTiles; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bar_s[2 * t + b], 1);
-        mbar_init(&bar_p[2 * t + b], 4);
-        mbar_init(&bar_o[2 * t + b], 1);
-      }
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 4);
+      mbar_init(&bar_o[t], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -310,11 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (lane < pages_per_blk && blk < nblk) ? page_of(blk * pages_per_blk + lane) : 0;
   };
   // TMA of one key block's pages into its ring stage (whole loader warp)
-  auto load_blk = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* bars, int blk, int ids) {
-    const int st = blk % kStages;
+  auto load_blk = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* bars, int stages, int blk,
+                      int ids) {
+    const int st = blk % stages;
     if (lane == 0) mbar_arrive_expect_tx(&bars[st], kKVStageBytes);
 #pragma unroll
-    for (int i = 0; i < kNK / 16; ++i) {  // at most 4 pages per block (block_size >= 16)
+    for (int i = 0; i < kNK / 16; ++i) {  // at most 8 pages per block (block_size >= 16)
       const int pid = __shfl_sync(0xffffffffu, ids, i);
       if (lane == 0 && i < pages_per_blk) {
 #pragma unroll
@@ -325,17 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // a loader streams blocks 0 .. nblk-1 into its ring; block b reuses the
-  // stage of block b - kStages once `freed` says the MMAs reading it are done
-  auto run_loader = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* freed) {
-    constexpr int kLead = 4;  // page ids are read kLead blocks ahead
+  // stage of block b - stages once `freed` says the MMAs reading it are done
+  auto run_loader = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* freed,
+                        int stages) {
+    constexpr int kLead = 3;  // page ids are read kLead blocks ahead
     int ids[kLead];
 #pragma unroll
     for (int k = 0; k < kLead; ++k) ids[k] = fetch_ids(k);
     for (int b = 0; b < nblk; ++b) {
-      if (b >= kStages)
-        mbar_wait_bounded(&freed[b % kStages], uint32_t((b - kStages) / kStages) & 1, p.err,
+      if (b >= stages)
+        mbar_wait_bounded(&freed[b % stages], uint32_t((b - stages) / stages) & 1, p.err,
                           abort_flag);
-      load_blk(map, ring, full, b, ids[0]);
+      load_blk(map, ring, full, stages, b, ids[0]);
 #pragma unroll
       for (int k = 0; k + 1 < kLead; ++k) ids[k] = ids[k + 1];
       ids[kLead - 1] = fetch_ids(b + kLead);
@@ -351,88 +398,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sQ + t * kQBytes + dh * (kM * 128), &tm_q, dh * 64, 0, h,
                       q0 + tokA + t * TQ, bar_q);
     }
-    run_loader(&tm_k, sK, bar_k, bar_kfree);
+    run_loader(&tm_k, sK, bar_k, bar_kfree, kStagesK);
   } else if (warp == kVLoadWarp) {
-    run_loader(&tm_v, sV, bar_v, bar_vfree);
+    run_loader(&tm_v, sV, bar_v, bar_vfree, kStagesV);
   } else if (warp == kMmaWarp) {
     constexpr uint32_t kIdescS = idesc_bf16(kM, kNK, false);
     constexpr uint32_t kIdescO = idesc_bf16(kM, kD, true);
-    auto issue_s = [&](int t, int blk) {  // lane 0: S_t of block blk -> buffer blk & 1
+    auto issue_s = [&](int t, int blk) {  // lane 0: S_t of block blk
       const uint32_t qa = smem_u32(sQ + t * kQBytes);
-      const uint32_t ka = smem_u32(sK + (blk % kStages) * kKVStageBytes);
+      const uint32_t ka = smem_u32(sK + (blk % kStagesK) * kKVStageBytes);
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
         const int dh = ks >> 2, w = ks & 3;
         const uint64_t ad = sw128_desc(qa + dh * (kM * 128) + w * 32, 16, 1024);
         const uint64_t bd = sw128_desc(ka + dh * (kNK * 128) + w * 32, 16, 1024);
-        mma_bf16(tmem + kColS + (2 * t + (blk & 1)) * kNK, ad, bd, kIdescS, ks > 0);
+        mma_bf16(tmem + kColS + t * kNK, ad, bd, kIdescS, ks > 0);
       }
-      mma_commit(&bar_s[2 * t + (blk & 1)]);
+      mma_commit(&bar_s[t]);
     };
-    auto issue_pv = [&](int t, int blk) {  // lane 0: O_t += P_t(buffer blk & 1) V_blk
-      const uint32_t pa = smem_u32(sP + (2 * t + (blk & 1)) * kPBytes);
-      const uint32_t va = smem_u32(sV + (blk % kStages) * kKVStageBytes);
+    auto issue_pv = [&](int t, int blk, bool last) {  // lane 0: O_t += P_t V_blk
+      const uint32_t va = smem_u32(sV + (blk % kStagesV) * kKVStageBytes);
 #pragma unroll
       for (int ks = 0; ks < kNK / 16; ++ks) {
-        const uint64_t ad = sw128_desc(pa + ks * 32, 16, 1024);
         const uint64_t bd = sw128_desc(va + ks * 2048, kNK * 128, 1024);
-        mma_bf16(tmem + kColO + t * kD, ad, bd, kIdescO, (blk > 0 || ks > 0) ? 1u : 0u);
+        mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8, bd, kIdescO,
+                    (blk > 0 || ks > 0) ? 1u : 0u);
       }
-      mma_commit(&bar_o[2 * t + (blk & 1)]);
+      if (last) mma_commit(&bar_o[t]);
     };
     auto wait_k = [&](int b) {
-      mbar_wait_bounded(&bar_k[b % kStages], uint32_t(b / kStages) & 1, p.err, abort_flag);
+      mbar_wait_bounded(&bar_k[b % kStagesK], uint32_t(b / kStagesK) & 1, p.err, abort_flag);
     };
 
-    // S of blocks 0 and 1 (S runs two blocks ahead of the softmax)
     mbar_wait_bounded(bar_q, 0, p.err, abort_flag);
-    for (int b = 0; b < 2 && b < nblk; ++b) {
-      wait_k(b);
+    if (nblk > 0) {
+      wait_k(0);
       if (lane == 0) {
         tc_fence_after();
-        if (b < nb0) issue_s(0, b);
-        if (b < nb1) issue_s(1, b);
-        mma_commit(&bar_kfree[b % kStages]);
+        if (nb0 > 0) issue_s(0, 0);
+        if (nb1 > 0) issue_s(1, 0);
+        mma_commit(&bar_kfree[0]);
       }
       __syncwarp();
     }
     for (int j = 0; j < nblk; ++j) {
-      const int st = j % kStages;
+      const int sv = j % kStagesV;
       // V_j landed; rows past the sequence end may hold never-written slots:
       // zero them so that 0 * V stays 0 in the PV product
-      mbar_wait_bounded(&bar_v[st], uint32_t(j / kStages) & 1, p.err, abort_flag);
+      mbar_wait_bounded(&bar_v[sv], uint32_t(j / kStagesV) & 1, p.err, abort_flag);
       if (j * kNK + kNK > L) {
         const int first = max(0, L - j * kNK);
         for (int i = lane; i < (kNK - first) * 16; i += 32) {
           const int r = first + (i >> 4), dh = (i >> 3) & 1, chunk = i & 7;
-          *reinterpret_cast<uint4*>(sV + st * kKVStageBytes + dh * (kNK * 128) + r * 128 +
+          *reinterpret_cast<uint4*>(sV + sv * kKVStageBytes + dh * (kNK * 128) + r * 128 +
                                     chunk * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
       __syncwarp();
-      // O_t += P_t V_j once the softmax warps have written P_t; P_t also says
-      // S_t of block j has been read, so that buffer takes block j + 2
+      // per tile: O_t += P_t V_j once the softmax warps have written P_t, then
+      // S_t of block j + 1 into the same TMEM columns (the tensor core runs
+      // MMAs in issue order, so the PV has read P before S overwrites it)
+      bool k_ready = false;
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
         const int nbt = t == 0 ? nb0 : nb1;
         if (j >= nbt) continue;
-        mbar_wait_bounded(&bar_p[2 * t + (j & 1)], uint32_t(j >> 1) & 1, p.err, abort_flag);
+        mbar_wait_bounded(&bar_p[t], uint32_t(j) & 1, p.err, abort_flag);
         if (lane == 0) {
           tc_fence_after();
-          issue_pv(t, j);
+          issue_pv(t, j, j == nbt - 1);
         }
         __syncwarp();
-        if (j + 2 < nbt) {
-          wait_k(j + 2);
-          if (lane == 0) issue_s(t, j + 2);
+        if (j + 1 < nbt) {
+          if (!k_ready) {
+            wait_k(j + 1);
+            k_ready = true;
+          }
+          if (lane == 0) issue_s(t, j + 1);
           __syncwarp();
         }
       }
-      // stage release: V_j after both tiles' PV, K_{j+2} after both tiles' S
+      // stage release: V_j after both tiles' PV, K_{j+1} after both tiles' S
       if (lane == 0) {
-        mma_commit(&bar_vfree[st]);
-        if (j + 2 < nblk) mma_commit(&bar_kfree[(j + 2) % kStages]);
+        mma_commit(&bar_vfree[sv]);
+        if (j + 1 < nblk) mma_commit(&bar_kfree[(j + 1) % kStagesK]);
       }
       __syncwarp();
     }
@@ -441,41 +491,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;                        // tile of this warpgroup
     const int row = tid & 127;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t colO = kColO + t * kD;
+    const uint32_t colS = kColS + t * kNK, colO = kColO + t * kD;
     const int tok = tokA + t * TQ + row / G;
     const bool row_valid = (row / G) < (t == 0 ? ntok0 : ntok1);
     const int pos = row_valid ? L - C + tok : -1;  // keys 0 .. pos are visible
     const int minpos = L - C + tokA + t * TQ;      // first token of the tile
     const float qm = p.q_mult;                     // scale * log2(e) > 0
-    uint8_t* const prow0 = sP + 2 * t * kPBytes + row * 128;  // buffer 0; buffer 1 follows
     float m_used = -INFINITY, l_sum = 0.f;
     const int nb = t == 0 ? nb0 : nb1;
 
     for (int j = 0; j < nb; ++j) {
-      // S_t of block j sits in buffer j & 1 (the producer runs two blocks ahead)
-      mbar_wait_bounded(&bar_s[2 * t + (j & 1)], uint32_t(j >> 1) & 1, p.err, abort_flag);
+      mbar_wait_bounded(&bar_s[t], uint32_t(j) & 1, p.err, abort_flag);
+      __syncwarp();  // lanes leave the polling loop separately; the TMEM loads are collective
       tc_fence_after();
-      const uint32_t colS = kColS + (2 * t + (j & 1)) * kNK;
-      float sv[kNK];
-      tmem_ld32(tmem + lane_base + colS, sv);
-      tmem_ld32(tmem + lane_base + colS + 32, sv + 32);
       const int kbase = j * kNK;
-      if (!row_valid) {
+      const bool diag = kbase + kNK - 1 > minpos;   // causal mask inside this block
+      // The softmax is issue-bound: per score it spends half a 3-input max
+      // (pass 1), half a packed FMA, one ex2, half a packed add and half a
+      // bf16x2 conversion (pass 2); masks cost extra only in diagonal blocks.
+      // tcgen05.ld / st are warp-collective: every lane runs them, whatever
+      // its row (rows past the chunk compute unused values).
+      // pass 1: block max
+      float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kNK; ++c) sv[c] = -INFINITY;
-      } else if (kbase + kNK - 1 > minpos) {  // diagonal block: causal mask
+      for (int c = 0; c < kNK; c += 64) {
+        float sv[64];
+        tmem_ld64(tmem + lane_base + colS + c, sv);
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < kNK; ++c) sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
+          for (int i = 0; i < 64; ++i) sv[i] = (kbase + c + i <= pos) ? sv[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          ma = fmax3(ma, sv[i], sv[i + 1]);
+          mb = fmax3(mb, sv[i + 2], sv[i + 3]);
+        }
       }
-      // max as an 8-way tree (short dependency chains)
-      float m8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
-#pragma unroll
-      for (int c = 8; c < kNK; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mx *= qm;  // raw-score max -> log2 domain (qm > 0)
+      const float mx = row_valid ? fmaxf(ma, mb) * qm : -INFINITY;  // log2 domain (qm > 0)
       // lagged running max: move it only when the block max exceeds it by > 8
       float alpha = 1.f;
       if (mx > m_used + 8.f) {
@@ -483,69 +535,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
         l_sum *= alpha;
       }
-      // P = 2^(s * qm - m) -> bf16 pairs; the row sum stays in fp32
-      uint32_t pw[kNK / 2];
-      float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                        make_float2(0.f, 0.f)};
-      if (m_used != -INFINITY) {
-        const float negm = -m_used;
+      // pass 2: P = 2^(s * qm - m) as bf16 pairs over the first half of S's
+      // columns (chunk c's pairs land in columns c/2 .. c/2 + 15, all read)
+      const float negm = m_used != -INFINITY ? -m_used : 0.f;
+      const float2 qm2 = make_float2(qm, qm), nm2 = make_float2(negm, negm);
+      float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < kNK; c += 2) {
-          const float2 e2 = make_float2(fast_exp2(fmaf(sv[c], qm, negm)),
-                                        fast_exp2(fmaf(sv[c + 1], qm, negm)));
-          acc2[(c >> 1) & 3] = __fadd2_rn(acc2[(c >> 1) & 3], e2);
+      for (int c = 0; c < kNK; c += 32) {
+        float sv[32];
+        tmem_ld32(tmem + lane_base + colS + c, sv);
+        uint32_t pw[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x2 = __ffma2_rn(make_float2(sv[i], sv[i + 1]), qm2, nm2);
+          float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+          if (diag) {
+            e2.x = (kbase + c + i <= pos) ? e2.x : 0.f;
+            e2.y = (kbase + c + i + 1 <= pos) ? e2.y : 0.f;
+          }
+          acc2[(i >> 1) & 1] = __fadd2_rn(acc2[(i >> 1) & 1], e2);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
-          pw[c / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kNK / 2; ++c) pw[c] = 0u;
+        tmem_st16_async(tmem + lane_base + colS + c / 2, pw);
       }
-      const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
-      const float2 a = __fadd2_rn(a01, a23);
+      const float2 a = __fadd2_rn(acc2[0], acc2[1]);
       l_sum += a.x + a.y;
 
-      // P buffer j & 1 was last read by PV of block j - 2: wait for it.  A
-      // rescale of O needs every PV so far (block j - 1) to be done; it is rare
-      // (the running max moves by > 2^8 only early in a row).
-      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      if (rescale) {
-        mbar_wait_bounded(&bar_o[2 * t + ((j - 1) & 1)], uint32_t((j - 1) >> 1) & 1, p.err,
-                          abort_flag);
-      } else if (j > 1) {
-        mbar_wait_bounded(&bar_o[2 * t + (j & 1)], uint32_t((j - 2) >> 1) & 1, p.err, abort_flag);
-      }
-      if (j > 0) {
-        tc_fence_after();
-        // tcgen05.ld/st are warp-collective: the whole warp rescales (rows
-        // that do not need it multiply by 1)
-        if (rescale) {
+      // O rescale (rare: the running max moves by > 2^8 only early in a row).
+      // PV_{j-1} is complete: the commit behind "S_j ready" covers it.
+      // tcgen05.ld/st are warp-collective: the whole warp rescales (rows that
+      // do not need it multiply by 1).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < kD; cc += 32) {  // 32 columns at a time: bounded registers
-            float o[32];
-            tmem_ld32(tmem + lane_base + colO + cc, o);
+        for (int cc = 0; cc < kD; cc += 32) {  // 32 columns at a time: bounded registers
+          float o[32];
+          tmem_ld32(tmem + lane_base + colO + cc, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem + lane_base + colO + cc, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + lane_base + colO + cc, o);
         }
       }
-      uint8_t* const prow = prow0 + (j & 1) * kPBytes;
-#pragma unroll
-      for (int c8 = 0; c8 < kNK / 8; ++c8)
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
-            make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p[2 * t + (j & 1)]);
+      if (lane == 0) mbar_arrive(&bar_p[t]);
     }
 
     // ---- epilogue: O / l -> bf16 ----------------------------------------------------
     if (nb > 0) {
       // the last PV's commit also covers every earlier MMA of the producer
-      mbar_wait_bounded(&bar_o[2 * t + ((nb - 1) & 1)], uint32_t((nb - 1) >> 1) & 1, p.err,
-                        abort_flag);
+      mbar_wait_bounded(&bar_o[t], 0, p.err, abort_flag);
+      __syncwarp();
       tc_fence_after();
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
