@@ -491,6 +491,21 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
 }
 
 // ---- merge -------------------------------------------------------------------------
+// One warp per (sequence, q head) with more than one partition.  Lane k holds
+// partition k's (m, l): the warp takes M = max m and L = sum 2^(m - M) l with
+// shuffles, then every lane accumulates its D/32 output columns over the
+// partitions, four partial rows in flight at a time.
+template <int D>
+__device__ __forceinline__ void load_cols(const float* src, float (&v)[D / 32]) {
+  if constexpr (D == 128) {
+    const float4 x = *reinterpret_cast<const float4*>(src);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const float2 x = *reinterpret_cast<const float2*>(src);
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
   constexpr int DV = D / 32;
@@ -505,25 +520,54 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   const size_t prow = size_t(gw) * p.max_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + prow;
   float M = -INFINITY;
-  for (int k = 0; k < ns; ++k) M = fmaxf(M, ml[k].x);
+  for (int k = lane; k < ns; k += 32) M = fmaxf(M, ml[k].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float lsum = 0.f, a[DV];
 #pragma unroll
   for (int e = 0; e < DV; ++e) a[e] = 0.f;
   if (M != -INFINITY) {
-    for (int k = 0; k < ns; ++k) {
-      const float2 v = ml[k];
-      const float sw = fast_exp2(v.x - M);
-      lsum = fmaf(sw, v.y, lsum);
-      const float* src = p.ws_acc + (prow + k) * D + lane * DV;
+    for (int k0 = 0; k0 < ns; k0 += 32) {
+      float sw = 0.f;
+      if (k0 + lane < ns) {
+        const float2 v = ml[k0 + lane];
+        sw = fast_exp2(v.x - M);
+        lsum = fmaf(sw, v.y, lsum);
+      }
+      const int nk = min(32, ns - k0);
+      const float* base = p.ws_acc + (prow + k0) * D + lane * DV;
+      int i = 0;
+      for (; i + 4 <= nk; i += 4) {
+        float v0[DV], v1[DV], v2[DV], v3[DV];
+        load_cols<D>(base + (i + 0) * D, v0);
+        load_cols<D>(base + (i + 1) * D, v1);
+        load_cols<D>(base + (i + 2) * D, v2);
+        load_cols<D>(base + (i + 3) * D, v3);
+        const float w0 = __shfl_sync(0xffffffffu, sw, i);
+        const float w1 = __shfl_sync(0xffffffffu, sw, i + 1);
+        const float w2 = __shfl_sync(0xffffffffu, sw, i + 2);
+        const float w3 = __shfl_sync(0xffffffffu, sw, i + 3);
 #pragma unroll
-      for (int e = 0; e < DV; ++e) a[e] = fmaf(sw, src[e], a[e]);
+        for (int e = 0; e < DV; ++e)
+          a[e] = fmaf(w3, v3[e], fmaf(w2, v2[e], fmaf(w1, v1[e], fmaf(w0, v0[e], a[e]))));
+      }
+      for (; i < nk; ++i) {
+        float v0[DV];
+        load_cols<D>(base + i * D, v0);
+        const float w0 = __shfl_sync(0xffffffffu, sw, i);
+#pragma unroll
+        for (int e = 0; e < DV; ++e) a[e] = fmaf(w0, v0[e], a[e]);
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
   }
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + size_t(gw) * D + lane * DV;
   const int kvh = (gw - s * p.num_q_heads) / (p.num_q_heads / p.num_kv_heads);
   const float vm = p.v_scales ? p.v_mult * __ldg(p.v_scales + kvh) : p.v_mult;
+  const float inv = lsum > 0.f ? vm / lsum : 0.f;
 #pragma unroll
-  for (int e = 0; e < DV; ++e) dst[e] = __float2bfloat16_rn(lsum > 0.f ? a[e] / lsum * vm : 0.f);
+  for (int e = 0; e < DV; ++e) dst[e] = __float2bfloat16_rn(a[e] * inv);
 }
 
 // ---- host launch ----------------------------------------------------------------
