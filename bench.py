@@ -2,10 +2,12 @@
 
 Default workload: Llama-2-13B-shaped MHA decode layer (64 sequences, 40/40
 heads, head_dim 128, block size 64, context lengths U[128, 4096], bf16 KV,
-1.25x pool with permuted page ids).  One step = kv_append of the batch's new
-tokens + paged decode attention over the whole batch (planner, split-K decode,
-merge).  --workload selects another configuration (1..5); configuration 5 adds
-the chunked-prefill call to the step.
+1.25x pool with permuted page ids).  One step = the append of the batch's new
+tokens + paged decode attention over the whole batch, in one call
+(pkv_paged_attention_append: planning and append in one launch, split-K
+decode, merge); --separate-append makes it two calls (pkv_kv_append, then
+pkv_paged_attention).  --workload selects another configuration (1..5);
+configuration 5 adds the chunked-prefill call to the step.
 
 Prints ONE JSON line.  `value` = algorithmic bytes of the step / device time
 per step (K/V bytes streamed dominate: 2 * head_dim * element size per token
@@ -270,7 +272,9 @@ def _config(w, args):
          "partition_tokens": args.partition or "auto",
          "l2": "no flush: each step streams the whole KV set, far larger than the 129 MB L2",
          "parallelism": f"replicas x{args.gpus}",
-         "launch": "cuda_graph_replay" if args.graph else "eager"}
+         "launch": "cuda_graph_replay" if args.graph else "eager",
+         "step_calls": ("pkv_paged_attention_append" if args.fused else
+                        "pkv_kv_append + pkv_paged_attention")}
     if w.num_prefill:
         c["prefill_chunks"] = [int(x) for x in w.prefill_chunk_lens]
     return c
@@ -312,12 +316,19 @@ def run_gpu(args):
     def step(q, k_new, v_new, slots, bt, cl, qp=None, cu=None, pbt=None, pcl=None, ev=None,
              o=None, op=None):
         o = out if o is None else o
-        pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
-        if ev is not None:
-            ev[0].record(stream)
-        pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
-                            workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
-                            partition_tokens=args.partition)
+        if args.fused:  # the append runs inside the attention call's planning launch
+            if ev is not None:
+                ev[0].record(stream)
+            pkv.paged_attention_append(q, k_new, v_new, slots, kp, vp, bt, cl, w.max_context_len,
+                                       w.scale, out=o, workspace=ws, k_scale=w.k_scale,
+                                       v_scale=w.v_scale, partition_tokens=args.partition)
+        else:
+            pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
+            if ev is not None:
+                ev[0].record(stream)
+            pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
+                                workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
+                                partition_tokens=args.partition)
         if ev is not None:
             ev[1].record(stream)
         if has_prefill:
@@ -450,12 +461,15 @@ def run_gpu(args):
     attn_bytes = (w.decode_kv_bytes() + 2 * B * Hq * D * 2 +
                   int(np.sum((w.context_lens.astype(np.int64) + w.block_size - 1)
                              // w.block_size)) * 4 + B * 4)
+    if args.fused:  # the timed call also scatters the appended rows
+        attn_bytes += B * w.num_kv_heads * D * (2 * 2 + 2 * w.elem_bytes) + B * 8
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     # 4 or 8 q heads per kv head at head_dim 128 run on the tensor-core decode
     kname = ("decode_mma_kernel" if D == 128 and w.group in (4, 8) and w.block_size >= 16
              else "decode_kernel")
-    launches_per_step = 3 + (1 if has_prefill else 0)   # append, plan, decode (+ prefill)
+    launches_per_step = (2 if args.fused else 3) + (1 if has_prefill else 0)
+    # append, plan, decode (+ prefill); fused: plan-and-append, decode
     part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,
                                                 w.k_scale, w.v_scale)
     splits = max_splits > 1
@@ -469,7 +483,9 @@ def run_gpu(args):
         "frac_of_hbm_peak": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": f"{kname} (pkv_paged_attention: plan + decode + merge)",
+                     "kernel": (f"{kname} (pkv_paged_attention_append: plan and append + "
+                                "decode + merge)" if args.fused else
+                                f"{kname} (pkv_paged_attention: plan + decode + merge)"),
                      "algorithmic_bytes_per_launch": attn_bytes,
                      "traffic": _ncu_traffic(kname, w.name)},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
@@ -507,6 +523,9 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition tokens (0 = library's automatic choice)")
+    ap.add_argument("--separate-append", dest="fused", action="store_false",
+                    help="two calls per decode step (pkv_kv_append, then pkv_paged_attention) "
+                         "instead of pkv_paged_attention_append")
     ap.add_argument("--graph", action="store_true",
                     help="capture the step in a CUDA graph and time its replays")
     ap.add_argument("--num-seqs", type=int, default=None,

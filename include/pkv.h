@@ -238,6 +238,24 @@ PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
  * thread (explains PKV_ERR_CUDA; "no error" if none).  Never NULL. */
 PKV_API const char *pkv_last_cuda_error(void);
 
+/* One decode step in one call: the same result as pkv_kv_append(k_new, v_new,
+ * slot_mapping, num_new_tokens, ...) followed by pkv_paged_attention(...) on
+ * the same stream, with the append fused into the attention's planning
+ * launch (one kernel launch fewer per step).  Arguments as in those two
+ * calls (k_new / v_new: device bf16 [num_new_tokens][Hkv][D]; slot_mapping:
+ * device int64 [num_new_tokens], slot < 0 = padding); the appended tokens are
+ * visible to the attention (context_lens count them).  The workspace is the
+ * same as pkv_paged_attention's.  num_new_tokens = 0 is a plain
+ * pkv_paged_attention; num_seqs = 0 a plain pkv_kv_append.  Errors: any status
+ * of either call, returned before anything is enqueued when it comes from
+ * host validation. */
+PKV_API pkv_status pkv_paged_attention_append(
+    const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+    int32_t num_new_tokens, void *k_pool, void *v_pool, const pkv_pool_desc *pool,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale,
+    int32_t partition_tokens, void *workspace, size_t workspace_bytes, void *out, void *stream);
+
 /* Copy whole blocks for copy-on-write of shared prefix pages (the page's
  * §4.1 / §4.2: blocks are reused and shared between sequences; a shared
  * block must be duplicated before one of its owners writes into it).

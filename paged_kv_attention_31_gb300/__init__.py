@@ -11,6 +11,7 @@ Functions mirror the C entry points:
     paged_attention_plan            <- pkv_paged_attention_plan
     paged_attention                 <- pkv_paged_attention
     paged_attention_noalloc         <- pkv_paged_attention_noalloc
+    paged_attention_append          <- pkv_paged_attention_append (append fused in)
     paged_prefill                   <- pkv_paged_prefill
     copy_blocks                     <- pkv_copy_blocks
     KVCacheManager                  <- pkv_cache_* (host page manager)
@@ -81,6 +82,9 @@ def lib():
             L.pkv_paged_attention.restype = i32
             L.pkv_paged_attention.argtypes = [vp, vp, vp, pd, vp, i32, vp, i32, i32, i32, f32,
                                               i32, vp, sz, vp, vp]
+            L.pkv_paged_attention_append.restype = i32
+            L.pkv_paged_attention_append.argtypes = [vp, vp, vp, vp, i32, vp, vp, pd, vp, i32, vp,
+                                                     i32, i32, i32, f32, i32, vp, sz, vp, vp]
             L.pkv_paged_attention_noalloc.restype = i32
             L.pkv_paged_attention_noalloc.argtypes = [vp, vp, vp, pd, vp, i32, vp, i32, i32, i32,
                                                       f32, i32, vp, vp]
@@ -247,6 +251,41 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_l
                                      int(workspace.numel() * workspace.element_size()),
                                      _ptr(out), _stream(stream)),
            "pkv_paged_attention")
+    return out
+
+
+def paged_attention_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                           context_lens, max_context_len, scale, out=None, workspace=None,
+                           k_scale=1.0, v_scale=1.0, partition_tokens=0, stream=None,
+                           k_scales=None, v_scales=None) -> torch.Tensor:
+    """kv_append + paged_attention in one call (the append runs in the
+    attention's planning launch).  Returns out [B, Hq, D] bf16."""
+    if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16:
+        raise TypeError("k_new / v_new must be bfloat16")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if q.dtype != torch.bfloat16 or q.dim() != 3:
+        raise TypeError("q must be bfloat16 [num_seqs, num_q_heads, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables / context_lens must be int32")
+    desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
+    if v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("k_pool and v_pool differ")
+    T = int(slot_mapping.shape[0])
+    if tuple(k_new.shape) != (T, desc.num_kv_heads, desc.head_dim) or k_new.shape != v_new.shape:
+        raise ValueError("k_new / v_new must be [T, num_kv_heads, head_dim]")
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool, partition_tokens,
+                                                k_scale, v_scale)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().pkv_paged_attention_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(k_pool), _ptr(v_pool),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        B, Hq, int(max_context_len), float(scale), int(partition_tokens), _ptr(workspace),
+        workspace.numel(), _ptr(out), _stream(stream)), "pkv_paged_attention_append")
     return out
 
 

@@ -31,6 +31,7 @@
 //        (q is pre-multiplied by scale*log2(e)), p = 2^(s - m).
 //   PV   each lane owns D/32 output columns of all G heads; p is broadcast
 //        from shared memory.
+#include "pkv_append.cuh"
 #include "pkv_common.cuh"
 #include "pkv_launch.h"
 
@@ -185,12 +186,12 @@ __device__ __forceinline__ int effective_len(int L, int cap, int32_t* err) {
 }
 
 // ---- planner --------------------------------------------------------------------
-__global__ void __launch_bounds__(512) decode_plan_kernel(const DecodeParams p) {
+// Counting sort of the (sequence, partition) items by length, longest first,
+// and reset of the work counter; one CTA of 512 threads.
+__device__ void plan_items(const DecodeParams& p) {
   __shared__ int hist[kMaxBuckets];
   __shared__ int offs[kMaxBuckets];
   const int nb = p.partition / kTT + 1;  // bucket = tiles in the item (0 .. partition/TT)
-  pdl_launch_dependents();
-  pdl_wait();  // the step's kv_append (and anything before it) is done
   for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
@@ -221,6 +222,25 @@ __global__ void __launch_bounds__(512) decode_plan_kernel(const DecodeParams p) 
       p.items[idx] = make_int2(s, k);
     }
   }
+}
+
+__global__ void __launch_bounds__(512) decode_plan_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the step's kv_append (and anything before it) is done
+  plan_items(p);
+}
+
+// The decode step's append fused into the planning launch: CTA 0 plans and
+// every CTA scatters its share of the new rows.  The planner reads only the
+// context lengths, which the append does not write; the decode kernels wait
+// for this whole grid (griddepcontrol.wait), so they see every appended row.
+template <bool FP8>
+__global__ void __launch_bounds__(512) decode_plan_append_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // earlier kernels of the stream (readers of the pool) are done
+  if (blockIdx.x == 0) plan_items(p);
+  append_rows<FP8>(p.append, int64_t(blockIdx.x) * blockDim.x + threadIdx.x,
+                   int64_t(gridDim.x) * blockDim.x);
 }
 
 // ---- decode -----------------------------------------------------------------------
@@ -603,8 +623,7 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) 
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NTHR, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  if ((e = launch_pdl(decode_plan_kernel, dim3(1), dim3(512), 0, stream, p)) != cudaSuccess)
-    return e;
+  if ((e = launch_decode_plan(p, num_sms, stream)) != cudaSuccess) return e;
   if ((e = launch_pdl(kern, dim3(num_sms * per_sm), dim3(C::NTHR), smem, stream, p)) !=
       cudaSuccess)
     return e;
@@ -629,8 +648,17 @@ cudaError_t launch_g(const DecodeParams& p, int num_sms, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t stream) {
-  return launch_pdl(decode_plan_kernel, dim3(1), dim3(512), 0, stream, p);
+cudaError_t launch_decode_plan(const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  if (!p.fuse_append) return launch_pdl(decode_plan_kernel, dim3(1), dim3(512), 0, stream, p);
+  const int64_t chunks = int64_t(p.append.num_tokens) * p.append.num_kv_heads * (p.head_dim / 8);
+  int64_t blocks = (chunks + 511) / 512;
+  if (blocks > int64_t(num_sms) * 4) blocks = int64_t(num_sms) * 4;
+  if (blocks < 1) blocks = 1;
+  return p.append.fp8
+             ? launch_pdl(decode_plan_append_kernel<true>, dim3(unsigned(blocks)), dim3(512), 0,
+                          stream, p)
+             : launch_pdl(decode_plan_append_kernel<false>, dim3(unsigned(blocks)), dim3(512), 0,
+                          stream, p);
 }
 
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {

@@ -497,7 +497,7 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  if ((e = launch_decode_plan(p, stream)) != cudaSuccess) return e;
+  if ((e = launch_decode_plan(p, num_sms, stream)) != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms * per_sm), dim3(kNW * 32), smem, stream, tk, tv, p);
   if (e != cudaSuccess) return e;
   if (p.max_splits > 1 && (e = launch_decode_merge(p, stream)) != cudaSuccess) return e;

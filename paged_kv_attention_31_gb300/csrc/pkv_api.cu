@@ -119,6 +119,35 @@ const char* pkv_status_string(int32_t s) {
   }
 }
 
+// Validated append parameters (status before anything is enqueued).
+static pkv_status make_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                              int32_t num_tokens, void* k_pool, void* v_pool,
+                              const pkv_pool_desc* pool, pkv::AppendParams* p, int32_t* err) {
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
+    return PKV_ERR_INVALID_ARG;
+  p->k_new = k_new;
+  p->v_new = v_new;
+  p->slot_mapping = slot_mapping;
+  p->k_pool = k_pool;
+  p->v_pool = v_pool;
+  p->num_slots = int64_t(pool->num_blocks) * pool->block_size;
+  p->num_tokens = num_tokens;
+  p->num_kv_heads = pool->num_kv_heads;
+  p->block_size = pool->block_size;
+  p->head_dim = pool->head_dim;
+  p->k_scale = pool->k_scale;
+  p->v_scale = pool->v_scale;
+  const bool fp8_pool = pool->kv_dtype == PKV_KV_FP8_E4M3;
+  p->k_scales = fp8_pool ? pool->k_scales : nullptr;
+  p->v_scales = fp8_pool ? pool->v_scales : nullptr;
+  p->fp8 = fp8_pool;
+  p->err = err;
+  return PKV_OK;
+}
+
 pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                          int32_t num_tokens, void* k_pool, void* v_pool,
                          const pkv_pool_desc* pool, void* stream) {
@@ -126,29 +155,12 @@ pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* sl
   if (st != PKV_OK) return st;
   if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
-  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
-      (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
-    return PKV_ERR_INVALID_ARG;
+  pkv::AppendParams p;
+  if ((st = make_append(k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, pool, &p,
+                        nullptr)) != PKV_OK)
+    return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PKV_OK) return st;
-  pkv::AppendParams p;
-  p.k_new = k_new;
-  p.v_new = v_new;
-  p.slot_mapping = slot_mapping;
-  p.k_pool = k_pool;
-  p.v_pool = v_pool;
-  p.num_slots = int64_t(pool->num_blocks) * pool->block_size;
-  p.num_tokens = num_tokens;
-  p.num_kv_heads = pool->num_kv_heads;
-  p.block_size = pool->block_size;
-  p.head_dim = pool->head_dim;
-  p.k_scale = pool->k_scale;
-  p.v_scale = pool->v_scale;
-  const bool fp8_pool = pool->kv_dtype == PKV_KV_FP8_E4M3;
-  p.k_scales = fp8_pool ? pool->k_scales : nullptr;
-  p.v_scales = fp8_pool ? pool->v_scales : nullptr;
-  p.fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
   p.err = dev->err;
   return from_cuda(pkv::launch_kv_append(p, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -213,12 +225,15 @@ pkv_status pkv_paged_attention_plan(int32_t num_seqs, int32_t num_q_heads,
   return PKV_OK;
 }
 
-pkv_status pkv_paged_attention(const void* q, const void* k_pool, const void* v_pool,
-                               const pkv_pool_desc* pool, const int32_t* block_tables,
-                               int32_t max_blocks_per_seq, const int32_t* context_lens,
-                               int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
-                               float scale, int32_t partition_tokens, void* workspace,
-                               size_t workspace_bytes, void* out, void* stream) {
+// Decode attention; with `app`, the step's appends run in the planning launch.
+static pkv_status paged_attention_impl(const void* q, const void* k_pool, const void* v_pool,
+                                       const pkv_pool_desc* pool, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t max_context_len, float scale,
+                                       int32_t partition_tokens, void* workspace,
+                                       size_t workspace_bytes, void* out, void* stream,
+                                       const pkv::AppendParams* app) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || max_blocks_per_seq <= 0)
@@ -281,7 +296,48 @@ pkv_status pkv_paged_attention(const void* q, const void* k_pool, const void* v_
   p.v_scales = fp8 ? pool->v_scales : nullptr;
   p.q_mult = scale * (fp8 && !p.k_scales ? pool->k_scale : 1.0f) * 1.4426950408889634f;
   p.v_mult = fp8 && !p.v_scales ? pool->v_scale : 1.0f;
+  p.fuse_append = app != nullptr;
+  if (app) {
+    p.append = *app;
+    p.append.err = dev->err;
+  }
   return from_cuda(pkv::launch_decode(p, fp8, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attention(const void* q, const void* k_pool, const void* v_pool,
+                               const pkv_pool_desc* pool, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                               float scale, int32_t partition_tokens, void* workspace,
+                               size_t workspace_bytes, void* out, void* stream) {
+  return paged_attention_impl(q, k_pool, v_pool, pool, block_tables, max_blocks_per_seq,
+                              context_lens, num_seqs, num_q_heads, max_context_len, scale,
+                              partition_tokens, workspace, workspace_bytes, out, stream, nullptr);
+}
+
+pkv_status pkv_paged_attention_append(const void* q, const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, int32_t num_new_tokens,
+                                      void* k_pool, void* v_pool, const pkv_pool_desc* pool,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_context_len, float scale,
+                                      int32_t partition_tokens, void* workspace,
+                                      size_t workspace_bytes, void* out, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_new_tokens < 0) return PKV_ERR_INVALID_ARG;
+  pkv::AppendParams app;
+  if (num_new_tokens > 0 &&
+      (st = make_append(k_new, v_new, slot_mapping, num_new_tokens, k_pool, v_pool, pool, &app,
+                        nullptr)) != PKV_OK)
+    return st;
+  if (num_seqs == 0)  // nothing to attend: the append alone
+    return pkv_kv_append(k_new, v_new, slot_mapping, num_new_tokens, k_pool, v_pool, pool,
+                         stream);
+  return paged_attention_impl(q, k_pool, v_pool, pool, block_tables, max_blocks_per_seq,
+                              context_lens, num_seqs, num_q_heads, max_context_len, scale,
+                              partition_tokens, workspace, workspace_bytes, out, stream,
+                              num_new_tokens > 0 ? &app : nullptr);
 }
 
 pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const void* k_pool,

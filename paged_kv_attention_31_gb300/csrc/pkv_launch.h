@@ -67,6 +67,10 @@ struct DecodeParams {
   float v_mult;                 // v_scale (FP8, per tensor) or 1
   const float* k_scales;        // optional per-kv-head FP8 scales, multiplied in per head
   const float* v_scales;
+  // pkv_paged_attention_append: this step's appends, done by the planning
+  // launch (every CTA scatters rows; CTA 0 also plans)
+  int32_t fuse_append;
+  AppendParams append;
 };
 
 struct PrefillParams {
@@ -120,7 +124,7 @@ struct CopyParams {
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, int num_sms, cudaStream_t stream);
 // split planner and partial merge of the decode (decode.cu)
-cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_plan(const DecodeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
 // head_dim 128, 4 or 8 q heads per kv head, bf16 or FP8 KV (decode_mma.cu)
 cudaError_t launch_decode_mma(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);

@@ -107,6 +107,20 @@ def test_copy_blocks_validation_before_any_cuda_call(lib):
     assert lib.pkv_copy_blocks(one, one, ctypes.byref(d), ctypes.c_void_p(258), 2, z) == 1
 
 
+def test_fused_append_validation_before_any_cuda_call(lib):
+    d = _desc()
+    z = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    args = lambda T, kn=one, slots=one: (one, kn, one, slots, T, one, one, ctypes.byref(d), one, 4,
+                                         one, 2, 8, 100, 0.1, 0, one, 1 << 20, one, z)
+    assert lib.pkv_paged_attention_append(*args(-1)) == 1            # negative token count
+    assert lib.pkv_paged_attention_append(*args(3, kn=z)) == 1       # null k_new
+    assert lib.pkv_paged_attention_append(*args(3, slots=ctypes.c_void_p(260))) == 1  # misaligned
+    bad = _desc(head_dim=96)
+    assert lib.pkv_paged_attention_append(one, one, one, one, 3, one, one, ctypes.byref(bad), one,
+                                          4, one, 2, 8, 100, 0.1, 0, one, 1 << 20, one, z) == 2
+
+
 def test_workspace_size_is_positive(lib):
     d = _desc()
     assert lib.pkv_paged_attention_workspace_size(4, 8, 1000, 0, ctypes.byref(d)) > 0
