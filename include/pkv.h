@@ -7,17 +7,24 @@
  * (§4.2 "KV缓存管理细节"), a per-sequence block table maps logical pages to
  * physical ones (§6.2 "Paged Attention优化": block_tables
  * [num_seqs, max_blocks]), sequences may share prefix pages (§6.2, the
- * list of its optimisations), the KV cache may be stored quantised and is dequantised
- * inside the attention kernel (§7.2 "KV Cache量化"), and long prompts are
- * processed as chunks interleaved with decode requests (§5.3 "分块上下文处理").
+ * list of its optimisations), the KV cache may be stored quantised and is
+ * dequantised inside the attention kernel (§7.2 "KV Cache量化"), and long
+ * prompts are processed as chunks interleaved with decode requests (§5.3
+ * "分块上下文处理").
  *
  * Conventions for every entry point
  *  - Pointers named as device data are device memory owned by the caller;
  *    descriptors (pkv_pool_desc) are host memory.  The library allocates no
- *    memory: scratch space (workspace) is sized by a query and passed in.
+ *    device memory at run time: scratch space (workspace) is sized by a query
+ *    and passed in (pkv_paged_attention_noalloc instead uses a fixed array
+ *    held from load time).  The host page manager (pkv_cache_*) keeps its
+ *    own state in host memory.
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
  *    is the legacy default stream), in stream order.  Nothing synchronises
- *    the host except pkv_get_device_error.
+ *    the host except pkv_get_device_error.  Kernels are launched with
+ *    programmatic stream serialization so that consecutive kernels overlap
+ *    their launch; each waits for the earlier kernels of the stream before
+ *    touching memory they use, so the ordering is that of plain launches.
  *  - Arguments are validated on the host before anything is enqueued;
  *    an invalid call returns an error and enqueues nothing.
  *  - Device data (block-table entries, context lengths, slots) is not read by

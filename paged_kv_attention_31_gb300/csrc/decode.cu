@@ -8,9 +8,11 @@
 // library's own addition for load balance on 152 SMs.
 //
 // Work decomposition
-//   * planner (1 CTA): for every sequence, nsplit = 1 if L <= partition else
-//     ceil(L / partition); emits the (sequence, partition) items sorted by
-//     size, longest first, and resets the work-fetch counter.
+//   * planner (CTA 0 of the planning launch): for every sequence, nsplit = 1
+//     if L <= partition else ceil(L / partition); emits the (sequence,
+//     partition) items sorted by size, longest first, and resets the
+//     work-fetch counter.  For pkv_paged_attention_append every CTA of that
+//     launch also scatters its share of the step's new K/V rows.
 //   * decode (persistent, #SM x occupancy CTAs of NW warps): a CTA takes work
 //     units (item, kv head) from an atomic counter.  All G = Hq/Hkv q heads of
 //     a kv head are packed in the unit, so each K/V page is read from HBM once
@@ -21,7 +23,11 @@
 //     warp states are combined in shared memory at the end of the unit and
 //     written either as the final bf16 output (one partition) or as an
 //     unnormalised partial (m, l, acc[D]) to the workspace.
-//   * merge: out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
+//   * merge (separate kernel, one warp per split row):
+//     out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
+// The planning launch, the decode and the merge are chained with
+// programmatic dependent launch: each waits (griddepcontrol.wait) for the
+// previous grid before touching its output.
 //
 // Inner tile (per warp, TT tokens):
 //   QK   TPT lanes per token, E head_dim elements per lane, G q heads packed;
