@@ -52,8 +52,14 @@ def _peaks():
 
 
 def _src_hash(name):
+    """sha256 prefix of a kernel source with comments and blank space taken
+    out, so that editing a comment does not invalidate a capture."""
     path = os.path.join(ROOT, "paged_kv_attention_31_gb300", "csrc", name)
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:12]
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode("utf-8")).hexdigest()[:12]
 
 
 def _ncu_traffic(kernel, workload_name):
