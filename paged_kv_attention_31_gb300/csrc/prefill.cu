@@ -148,22 +148,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 32 columns without waiting: the registers may be used only after
-// tmem_wait_ld_regs() on the same array (which ties the wait to them).
-__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   uint32_t r[32];
 #pragma unroll
@@ -527,22 +511,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bf16x2 conversion (pass 2); masks cost extra only in diagonal blocks.
       // tcgen05.ld / st are warp-collective: every lane runs them, whatever
       // its row (rows past the chunk compute unused values).
-      // pass 1: block max (one 128-column load)
-      float ma = -INFINITY, mb = -INFINITY;
-      {
-        float sv[kNK];
-        tmem_ld128(tmem + lane_base + colS, sv);
-        if (diag) {
+      // The block's 128 scores in one tcgen05.ld, kept in registers for both
+      // passes: the max (four independent chains of 3-input max) and P.
+      float sv[kNK];
+      tmem_ld128(tmem + lane_base + colS, sv);
+      if (diag) {
 #pragma unroll
-          for (int i = 0; i < kNK; ++i) sv[i] = (kbase + i <= pos) ? sv[i] : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < kNK; i += 4) {
-          ma = fmax3(ma, sv[i], sv[i + 1]);
-          mb = fmax3(mb, sv[i + 2], sv[i + 3]);
-        }
+        for (int i = 0; i < kNK; ++i) sv[i] = (kbase + i <= pos) ? sv[i] : -INFINITY;
       }
-      const float mx = row_valid ? fmaxf(ma, mb) * qm : -INFINITY;  // log2 domain (qm > 0)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < kNK; i += 8) {
+        m4[0] = fmax3(m4[0], sv[i], sv[i + 1]);
+        m4[1] = fmax3(m4[1], sv[i + 2], sv[i + 3]);
+        m4[2] = fmax3(m4[2], sv[i + 4], sv[i + 5]);
+        m4[3] = fmax3(m4[3], sv[i + 6], sv[i + 7]);
+      }
+      const float mx = row_valid ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qm
+                                 : -INFINITY;  // log2 domain (qm > 0)
       // lagged running max: move it only when the block max exceeds it by > 8
       float alpha = 1.f;
       if (mx > m_used + 8.f) {
@@ -550,46 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
         l_sum *= alpha;
       }
-      // pass 2: P = 2^(s * qm - m) as bf16 pairs over the first half of S's
-      // columns, 32 scores at a time; the next chunk's load is in flight
-      // while this one computes (chunk c's pairs land in columns c/2 ..
-      // c/2 + 15, all read already; the loads in flight read columns >= c + 32)
+      // P = 2^(s * qm - m) as bf16 pairs over the first half of S's columns
+      // (chunk c's pairs land in columns c/2 .. c/2 + 15; S is already in
+      // registers); masked scores are -inf and give 0
       const float negm = m_used != -INFINITY ? -m_used : 0.f;
       const float2 qm2 = make_float2(qm, qm), nm2 = make_float2(negm, negm);
       float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      auto p_chunk = [&](const uint32_t (&r)[32], int c) {
+#pragma unroll
+      for (int c = 0; c < kNK; c += 32) {
         uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                       qm2, nm2);
-          float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
-          if (diag) {
-            e2.x = (kbase + c + i <= pos) ? e2.x : 0.f;
-            e2.y = (kbase + c + i + 1 <= pos) ? e2.y : 0.f;
-          }
+          const float2 x2 = __ffma2_rn(make_float2(sv[c + i], sv[c + i + 1]), qm2, nm2);
+          const float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
           acc2[(i >> 1) & 1] = __fadd2_rn(acc2[(i >> 1) & 1], e2);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
           pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
         }
         tmem_st16_async(tmem + lane_base + colS + c / 2, pw);
-      };
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32_async(tmem + lane_base + colS, r0);
-        tmem_wait_ld_regs(r0);
-        tmem_ld32_async(tmem + lane_base + colS + 32, r1);
-        p_chunk(r0, 0);
-        tmem_wait_ld_regs(r1);
-        tmem_ld32_async(tmem + lane_base + colS + 64, r0);
-        p_chunk(r1, 32);
-        tmem_wait_ld_regs(r0);
-        tmem_ld32_async(tmem + lane_base + colS + 96, r1);
-        p_chunk(r0, 64);
-        tmem_wait_ld_regs(r1);
-        p_chunk(r1, 96);
       }
-      static_assert(kNK == 128, "pass 2 is written out for four 32-column chunks");
       const float2 a = __fadd2_rn(acc2[0], acc2[1]);
       l_sum += a.x + a.y;
 
