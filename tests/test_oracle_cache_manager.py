@@ -216,3 +216,21 @@ def test_random_operations_read_back_and_conserve(seed):
                 assert st == (ERR_INVALID_ARG if need < 0 else ERR_OUT_OF_BLOCKS)
         conservation(m)
         sim.check(m)
+
+
+def test_oracle_copy_blocks_duplicates_whole_blocks_only():
+    # the device copy-on-write's oracle: destination blocks become exact
+    # copies of their sources in both pools (every kv head, every slot);
+    # no other block changes
+    import oracle
+    rng = np.random.default_rng(9)
+    kp = rng.integers(0, 1 << 16, (7, 3, 4, 8)).astype(np.uint16)
+    vp = rng.integers(0, 1 << 16, (7, 3, 4, 8)).astype(np.uint16)
+    k0, v0 = kp.copy(), vp.copy()
+    oracle.copy_blocks(kp, vp, np.array([[1, 5], [3, 6]], np.int32))
+    assert np.array_equal(kp[5], k0[1]) and np.array_equal(vp[5], v0[1])
+    assert np.array_equal(kp[6], k0[3]) and np.array_equal(vp[6], v0[3])
+    for b in (0, 1, 2, 3, 4):
+        assert np.array_equal(kp[b], k0[b]) and np.array_equal(vp[b], v0[b])
+    oracle.copy_blocks(kp, vp, np.zeros((0, 2), np.int32))    # no pairs: no change
+    assert np.array_equal(kp[6], k0[3])
