@@ -75,7 +75,7 @@ typedef enum pkv_kv_dtype {
 } pkv_kv_dtype;
 
 /* Shape of the paged pool.  head_dim in {64, 128}; block_size in
- * {16, 32, 64}.  FP8 only: one scale per tensor (k_scale / v_scale, > 0 and
+ * {16, 32, 64, 128}.  FP8 only: one scale per tensor (k_scale / v_scale, > 0 and
  * finite), or one per kv head as the page's KV-cache quantisation section
  * describes (§7.2 "KV Cache量化", its first item): k_scales / v_scales,
  * optional device arrays of num_kv_heads positive finite floats (4-byte

@@ -47,7 +47,8 @@ pkv_status check_pool(const pkv_pool_desc* pool) {
   if (pool->kv_dtype != PKV_KV_BF16 && pool->kv_dtype != PKV_KV_FP8_E4M3)
     return PKV_ERR_INVALID_ARG;
   if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (pool->block_size != 16 && pool->block_size != 32 && pool->block_size != 64)
+  if (pool->block_size != 16 && pool->block_size != 32 && pool->block_size != 64 &&
+      pool->block_size != 128)
     return PKV_ERR_UNSUPPORTED;
   if (pool->kv_dtype == PKV_KV_FP8_E4M3) {
     if (!pool->k_scales && (!(pool->k_scale > 0.f) || !isfinite(pool->k_scale)))

@@ -68,7 +68,8 @@ def test_split_partitions_agree_with_oracle(partition):
 
 
 @pytest.mark.parametrize("G,D,P", [(1, 64, 16), (2, 128, 32), (4, 64, 64), (8, 128, 16),
-                                   (8, 64, 32), (1, 128, 64), (4, 128, 64), (8, 128, 32)])
+                                   (8, 64, 32), (1, 128, 64), (4, 128, 64), (8, 128, 32),
+                                   (1, 128, 128), (8, 128, 128), (2, 64, 128)])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
 def test_shapes_and_ragged_lengths(G, D, P, kv_dtype):
     # lengths around tile (16), page and partition boundaries, plus 0 and 1

@@ -16,7 +16,7 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("hkv,P,D", [(8, 32, 128), (3, 16, 64), (1, 64, 128)])
+@pytest.mark.parametrize("hkv,P,D", [(8, 32, 128), (3, 16, 64), (1, 64, 128), (2, 128, 128)])
 def test_kv_append_bit_exact(fp8, hkv, P, D):
     rng = np.random.default_rng(100 + hkv + P)
     nb, T = 37, 509

@@ -43,7 +43,8 @@ def test_small_mixed_config_every_row():
     _check(w, out)
 
 
-@pytest.mark.parametrize("G,P", [(1, 16), (2, 32), (4, 32), (8, 64), (4, 16), (16, 64)])
+@pytest.mark.parametrize("G,P", [(1, 16), (2, 32), (4, 32), (8, 64), (4, 16), (16, 64),
+                                 (4, 128), (8, 128)])
 def test_groups_blocks_and_ragged_chunks(G, P):
     # chunks of 1 token, whole-prompt chunks (prior 0), tails that end
     # mid-tile and mid-key-block
