@@ -222,8 +222,8 @@ PKV_API size_t pkv_paged_attention_noalloc_max_scratch(void);
  *   max_q_len       host upper bound of C_s
  *   scale           softmax scale, finite and > 0
  *   out             device, bf16 [num_q_tokens][num_q_heads][head_dim]
- * head_dim must be 128; the group size num_q_heads/num_kv_heads must divide
- * 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
+ * head_dim 64 or 128 and a bf16 pool (FP8 pools: PKV_ERR_UNSUPPORTED); the
+ * group size num_q_heads/num_kv_heads must divide 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
  */
 PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
                              const void *k_pool, const void *v_pool,

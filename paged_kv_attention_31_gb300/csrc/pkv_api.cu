@@ -349,7 +349,7 @@ pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const v
                              void* stream) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
-  if (pool->kv_dtype != PKV_KV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (pool->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || num_q_tokens < 0 ||
       max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;

@@ -46,7 +46,6 @@
 namespace pkv {
 namespace {
 
-constexpr int kD = 128;          // head_dim
 constexpr int kM = 128;          // query rows per tile
 constexpr int kNK = 128;         // keys per block
 constexpr int kTiles = 2;        // query tiles per CTA
@@ -58,27 +57,34 @@ constexpr int kKLoadWarp = kMmaWarp + 1;         // warp 9: TMA of Q and of the 
 constexpr int kVLoadWarp = kMmaWarp + 2;         // warp 10: TMA of the V ring
 constexpr int kThreads = kSoftmaxThreads + 3 * 32;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S (then P) of tile t at 128 t, O of tile t at 256 + 128 t
+// TMEM columns: S (then P) of tile t at 128 t, O of tile t at 256 + D t
 constexpr uint32_t kColS = 0, kColO = 256;
-
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int kQBytes = 2 * kM * 128;        // 32 KB per tile: two d-halves of [128 rows][128 B]
-constexpr int kKVStageBytes = 2 * kNK * 128; // 32 KB: two d-halves of [128 keys][128 B]
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTiles * kQBytes;
-constexpr int kOffV = kOffK + kStagesK * kKVStageBytes;
-constexpr int kOffBar = kOffV + kStagesV * kKVStageBytes;
 // barriers: q, k[SK], kfree[SK], v[SV], vfree[SV], s[tiles], p[tiles], o[tiles]
 constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
 // CTA order: end positions of up to kMaxRankGroups (sequence, tile pair) groups
 constexpr int kMaxRankGroups = 256;
-constexpr int kOffRank = kOffMisc + 16;
 // The 128-byte-swizzled tiles need a 1024-aligned base; dynamic shared memory
 // starts at least 128-aligned, so at most 896 bytes of padding are needed.
 constexpr int kMaxPad = 1024 - 128;
-constexpr int kSmemBytes = kOffRank + 4 * kMaxRankGroups + kMaxPad;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// Shared memory layout for head_dim D (offsets from a 1024-aligned base).
+// Rows of Q, K and V are split into D/64 halves of 64 bf16 (128 bytes, one
+// swizzle atom): a tile is [half][rows][128 B].
+template <int D>
+struct PfLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kHalves * kM * 128;         // per tile
+  static constexpr int kKVStageBytes = kHalves * kNK * 128;  // one key block of K or V
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTiles * kQBytes;
+  static constexpr int kOffV = kOffK + kStagesK * kKVStageBytes;
+  static constexpr int kOffBar = kOffV + kStagesV * kKVStageBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffRank = kOffMisc + 16;
+  static constexpr int kSmemBytes = kOffRank + 4 * kMaxRankGroups + kMaxPad;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kColO + kTiles * D <= kTmemCols, "TMEM budget");
+};
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -229,9 +235,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
 
 // The register file is handed out per group of four warps, so the 11-warp
 // CTA is budgeted as 12 warps: at most 168 registers per thread.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  constexpr int kD = D;
+  using Lay = PfLayout<D>;
+  constexpr int kHalves = Lay::kHalves, kQBytes = Lay::kQBytes;
+  constexpr int kKVStageBytes = Lay::kKVStageBytes;
+  constexpr int kOffQ = Lay::kOffQ, kOffK = Lay::kOffK, kOffV = Lay::kOffV;
+  constexpr int kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffRank = Lay::kOffRank;
   pdl_wait();  // inputs written by earlier kernels of the stream are visible
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pid = __shfl_sync(0xffffffffu, ids, i);
       if (lane == 0 && i < pages_per_blk) {
 #pragma unroll
-        for (int dh = 0; dh < 2; ++dh)
+        for (int dh = 0; dh < kHalves; ++dh)
           tma_load_4d(ring + st * kKVStageBytes + dh * (kNK * 128) + i * P * 128, map, dh * 64,
                       0, h, pid, &bars[st]);
       }
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar_q, kTiles * kQBytes);
       for (int t = 0; t < kTiles; ++t)
 #pragma unroll
-        for (int dh = 0; dh < 2; ++dh)
+        for (int dh = 0; dh < kHalves; ++dh)
           tma_load_4d(sQ + t * kQBytes + dh * (kM * 128), &tm_q, dh * 64, 0, h,
                       q0 + tokA + t * TQ, bar_q);
     }
@@ -448,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(&bar_v[sv], uint32_t(j / kStagesV) & 1, p.err, abort_flag);
       if (j * kNK + kNK > L) {
         const int first = max(0, L - j * kNK);
-        for (int i = lane; i < (kNK - first) * 16; i += 32) {
-          const int r = first + (i >> 4), dh = (i >> 3) & 1, chunk = i & 7;
+        for (int i = lane; i < (kNK - first) * 8 * kHalves; i += 32) {
+          const int r = first + i / (8 * kHalves), dh = (i / 8) % kHalves, chunk = i % 8;
           *reinterpret_cast<uint4*>(sV + sv * kKVStageBytes + dh * (kNK * 128) + r * 128 +
                                     chunk * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -616,14 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
-                           int num_sms, cudaStream_t stream) {
-  (void)num_sms;
-  if (p.head_dim != kD) return cudaErrorNotSupported;
+namespace {
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const void* v_pool,
+                             cudaStream_t stream) {
+  using Lay = PfLayout<D>;
   const int G = p.num_q_heads / p.num_kv_heads;
   if (G < 1 || kM % G != 0 || kNK % p.block_size != 0) return cudaErrorNotSupported;
   if (p.num_blocks >= (1 << 30)) return cudaErrorInvalidValue;
-  const uint64_t D = kD, P = p.block_size, Hkv = p.num_kv_heads, E = 2;
+  const uint64_t P = p.block_size, Hkv = p.num_kv_heads, E = 2;
   CUtensorMap tq, tk, tv;
   // q [T][Hkv][G][D] with box (64, G, 1, 128/G): rows ordered token-major, head-minor
   const auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -643,7 +658,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -652,9 +668,19 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const voi
       int64_t((p.tiles_per_seq + kTiles - 1) / kTiles) * p.num_kv_heads * p.num_seqs;
   if (ctas > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   const dim3 grid{static_cast<unsigned>(ctas)};
-  e = launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, p);
+  e = launch_pdl(prefill_kernel<D>, grid, dim3(kThreads), Lay::kSmemBytes, stream, tq, tk, tv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
+                           int num_sms, cudaStream_t stream) {
+  (void)num_sms;
+  if (p.head_dim == 128) return launch_prefill_d<128>(p, k_pool, v_pool, stream);
+  if (p.head_dim == 64) return launch_prefill_d<64>(p, k_pool, v_pool, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace pkv

@@ -86,12 +86,9 @@ def test_argument_validation_before_any_cuda_call(lib):
     assert lib.pkv_paged_attention(*args(3)) == 1
     assert lib.pkv_paged_attention(*args(4, part=24)) == 1     # not a multiple of block size
     assert lib.pkv_paged_attention(*args(4, ws=ctypes.c_void_p(272))) == 3  # misaligned workspace
-    # prefill: FP8 pools and head_dim 64 are not built
+    # prefill: FP8 pools are not built
     d8 = _desc(kv_dtype=1)
     assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d8), one, 4, one, 1, 4, 16, 16,
-                                 0.1, one, z) == 2
-    d64 = _desc(head_dim=64)
-    assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d64), one, 4, one, 1, 4, 16, 16,
                                  0.1, one, z) == 2
 
 

@@ -79,6 +79,20 @@ def test_many_chunks_cta_order(n_chunks):
                                 int(np.argmax(w.prefill_context_lens))}))
 
 
+@pytest.mark.parametrize("G,P", [(1, 16), (4, 32), (8, 64), (2, 128)])
+def test_head_dim_64(G, P):
+    priors = [0, 7, 64, 129, 0]
+    chunks = [1, 33, 200, 64, 257]
+    hkv = 2
+    w = W.make_mixed(f"prefill_d64_G{G}_P{P}", 1900 + G + P, [40], priors, chunks, hkv * G, hkv,
+                     64, P)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check(w, out)
+
+
 def test_never_written_slots_past_the_end_do_not_leak():
     # fill everything past each sequence's last token with NaN bit patterns
     w = W.make_mixed("prefill_nan_tail", 1234, [30], [5, 70], [50, 27], 32, 8, 128, 32)
