@@ -93,6 +93,21 @@ def test_head_dim_64(G, P):
     _check(w, out)
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_zero_length_chunks_in_the_batch(D):
+    # sequences with no query tokens this step (equal cu_seqlens entries) sit
+    # between real chunks: they own no output rows and disturb no other sequence
+    chunks = [64, 0, 129, 0, 1]
+    w = W.make_mixed(f"prefill_zero_chunks_d{D}", 5150, [20], [10, 300, 0, 5, 77], chunks,
+                     16, 4, D, 32)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    assert out.shape[0] == sum(chunks)
+    _check(w, out, seqs=[s for s in range(w.num_prefill) if chunks[s] > 0])
+
+
 def test_never_written_slots_past_the_end_do_not_leak():
     # fill everything past each sequence's last token with NaN bit patterns
     w = W.make_mixed("prefill_nan_tail", 1234, [30], [5, 70], [50, 27], 32, 8, 128, 32)
