@@ -385,7 +385,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(q, k_new, v_new, slots, bt, cl, qp=None, cu=None, pbt=None, pcl=None, ev=None,
-             o=None, op=None):
+             o=None, op=None, decode_only=False):
         o = out if o is None else o
         if args.fused:  # the append runs inside the attention call's planning launch
             if ev is not None:
@@ -402,7 +402,7 @@ def run_gpu(args):
                                 partition_tokens=args.partition)
         if ev is not None:
             ev[1].record(stream)
-        if has_prefill:
+        if has_prefill and not decode_only:
             if ev is not None:
                 ev[2].record(stream)
             pkv.paged_prefill(qp, cu, kp, vp, pbt, pcl, max_q, w.scale,
@@ -438,8 +438,11 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
 
     # --- timed region: device-resident inputs -------------------------------------
-    # A step whose working set is not well above the L2 would run from cache:
-    # then the L2 is flushed (a write of twice its size) before every step,
+    # The steps run back to back with no event between a step's calls: an
+    # event between two launches ends the programmatic launch chain (the next
+    # kernel could otherwise start while the previous one drains).  A step
+    # whose working set is not well above the L2 would run from cache: then
+    # the L2 is flushed (a write of twice its size) before every step,
     # outside the timed spans, and each step is timed on its own.
     flush_buf = None
     if args.flush:
@@ -463,17 +466,29 @@ def run_gpu(args):
         if graph is not None:
             graph.replay()
         else:
-            step(*args_dev, ev=evs[i])
+            step(*args_dev)
         if spans is not None:
             spans[i][1].record(stream)
     t_stop.record(stream)
     torch.cuda.synchronize(dev)
-    if graph is not None:  # per-call event timing from an eager pass
+    # per-call timing for the rooflines: the same steps again (eager), CUDA
+    # events on the launching stream around each call
+    for i in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(i & 255)
+        step(*args_dev, ev=evs[i])
+    torch.cuda.synchronize(dev)
+    # the mixed step's decode call alone, back to back (its launches chained)
+    dec_chain_ms = None
+    if has_prefill:
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
         for i in range(args.steps):
-            if flush_buf is not None:
-                flush_buf.fill_(i & 255)
-            step(*args_dev, ev=evs[i])
+            step(*args_dev, decode_only=True)
+        c1.record(stream)
         torch.cuda.synchronize(dev)
+        dec_chain_ms = c0.elapsed_time(c1) / args.steps
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
@@ -567,9 +582,15 @@ def run_gpu(args):
     attn_bytes = (w.decode_kv_bytes() + 2 * B * Hq * D * 2 +
                   int(np.sum((w.context_lens.astype(np.int64) + w.block_size - 1)
                              // w.block_size)) * 4 + B * 4)
-    if args.fused:  # the timed call also scatters the appended rows
-        attn_bytes += B * w.num_kv_heads * D * (2 * 2 + 2 * w.elem_bytes) + B * 8
+    if args.fused:  # the timed call also scatters the appended rows (all of them:
+        # with prefill chunks in the step, their rows too)
+        n_app = w.num_append_tokens
+        attn_bytes += n_app * w.num_kv_heads * D * (2 * 2 + 2 * w.elem_bytes) + n_app * 8
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    # the same call's time with its launches chained to the previous step's:
+    # the step itself when the call is the whole step, else a loop of the
+    # decode call alone
+    call_chain_ms = dec_chain_ms if has_prefill else ms
     peak = float(peaks["hbm_gbs"])
     # 4 or 8 q heads per kv head at head_dim 128 run on the tensor-core decode
     kname = ("decode_mma_kernel" if D == 128 and w.group in (4, 8) and w.block_size >= 16
@@ -592,8 +613,16 @@ def run_gpu(args):
                      "kernel": (f"{kname} (pkv_paged_attention_append: plan and append + "
                                 "decode + merge)" if args.fused else
                                 f"{kname} (pkv_paged_attention: plan + decode + merge)"),
-                     "algorithmic_bytes_per_launch": attn_bytes,
-                     "traffic": _ncu_traffic(kname, w.name)},
+                     "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": attn_ms,
+                     "timing": "CUDA events around each call (second pass over the steps)",
+                     "traffic": _ncu_traffic(kname, w.name),
+                     "back_to_back": {
+                         "ms_per_launch": call_chain_ms,
+                         "achieved": attn_bytes / (call_chain_ms * 1e-3) / 1e9,
+                         "frac": attn_bytes / (call_chain_ms * 1e-3) / 1e9 / peak,
+                         "timing": ("the decode call alone, launches chained, one event pair "
+                                    "around the loop" if has_prefill else
+                                    "the timed steps (the step is this call)")}},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -614,6 +643,7 @@ def run_gpu(args):
                             "unit": "TFLOP/s", "frac": tflops / tpeak, "peak_kind": peak_kind,
                             "kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
                             "algorithmic_flops_per_launch": flops, "ms_per_launch": prefill_ms,
+                            "timing": "CUDA events around each call (second pass over the steps)",
                             "traffic": _ncu_traffic("prefill_kernel", w.name)}
     if cpu_line is not None:
         line["cpu_baseline"], line["cpu_baseline_all_cores"] = cpu_line

@@ -44,6 +44,10 @@ def test_default_decode_line():
     assert d["roofline"]["bound"] == "hbm" and d["roofline"]["unit"] == "GB/s"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    ca = d["cpu_baseline_all_cores"]
+    assert ca["kind"] == "oracle" and ca["cores"] >= 1 and ca["value"] > 0 and ca["sample"]
+    b = d["roofline"]["back_to_back"]
+    assert b["ms_per_launch"] > 0 and abs(b["achieved"] / d["roofline"]["peak"] - b["frac"]) < 1e-9
 
 
 def test_mixed_step_line_reports_the_tensor_roofline():
@@ -51,3 +55,5 @@ def test_mixed_step_line_reports_the_tensor_roofline():
     _common(d)
     assert d["roofline"]["bound"] == "tensor" and d["roofline"]["unit"] == "TFLOP/s"
     assert d["decode_roofline"]["bound"] == "hbm"
+    assert d["decode_roofline"]["back_to_back"]["ms_per_launch"] > 0
+    assert d["tokens_per_s"] > 0
