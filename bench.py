@@ -350,6 +350,21 @@ def _config(w, args):
     return c
 
 
+def _packed(tensors, device):
+    """One uint8 buffer holding `tensors` back to back, each at a 256-byte
+    aligned offset (pinned when on the host), and views of it with the
+    tensors' dtypes and shapes: (buffer, views)."""
+    import torch
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(n, dtype=torch.uint8, device=device, pin_memory=(str(device) == "cpu"))
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for o, t in zip(offs, tensors)]
+    return buf, views
+
+
 def run_gpu(args):
     import torch
 
@@ -500,41 +515,46 @@ def run_gpu(args):
 
     # --- end to end through the public API from pinned host memory ------------------
     # Every step copies its inputs from pinned host memory and its outputs
-    # back.  Copies run on their own streams into double-buffered device
+    # back.  A step's inputs sit back to back in one pinned staging buffer and
+    # its outputs in one device buffer, so each step is one copy in and one
+    # copy out.  Copies run on their own streams into double-buffered device
     # inputs and outputs, so step i's copies overlap the kernels of step i - 1
     # (the kernels themselves stay in order on the compute stream: each
     # step's appends precede its attention).
-    host = [x.cpu().pin_memory() for x in args_dev]
     outs_dev = [out] + ([out_p] if has_prefill else [])
     nbuf = 2
-    sets = [[torch.empty_like(x) for x in args_dev] for _ in range(nbuf)]
-    osets = [[torch.empty_like(x) for x in outs_dev] for _ in range(nbuf)]
-    ohost = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs_dev]
-             for _ in range(nbuf)]
-    h2d = sum(x.numel() * x.element_size() for x in host)
-    d2h = sum(x.numel() * x.element_size() for x in outs_dev)
+    hbuf, hviews = _packed(args_dev, "cpu")
+    for hv, x in zip(hviews, args_dev):
+        hv.copy_(x.cpu())
+    dsets = [_packed(args_dev, dev) for _ in range(nbuf)]
+    osets = [_packed(outs_dev, dev) for _ in range(nbuf)]
+    ohost = [_packed(outs_dev, "cpu") for _ in range(nbuf)]
+    h2d = hbuf.numel()
+    d2h = osets[0][0].numel()
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(nbuf)]      # inputs of set b landed
     ev_done = [torch.cuda.Event() for _ in range(nbuf)]    # kernels done with set b
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]     # outputs of set b copied back
+
+    def run_set(b):
+        o = osets[b][1]
+        step(*dsets[b][1], o=o[0], op=o[1] if has_prefill else None)
 
     def e2e_step(i):
         b = i % nbuf
         if i >= nbuf:
             h2d_s.wait_event(ev_done[b])
         with torch.cuda.stream(h2d_s):
-            for hb, db in zip(host, sets[b]):
-                db.copy_(hb, non_blocking=True)
+            dsets[b][0].copy_(hbuf, non_blocking=True)
         ev_in[b].record(h2d_s)
         stream.wait_event(ev_in[b])
         if i >= nbuf:
             stream.wait_event(ev_out[b])
-        step(*sets[b], o=osets[b][0], op=osets[b][1] if has_prefill else None)
+        run_set(b)
         ev_done[b].record(stream)
         d2h_s.wait_event(ev_done[b])
         with torch.cuda.stream(d2h_s):
-            for hb, db in zip(ohost[b], osets[b]):
-                hb.copy_(db, non_blocking=True)
+            ohost[b][0].copy_(osets[b][0], non_blocking=True)
         ev_out[b].record(d2h_s)
 
     for i in range(min(args.warmup, 3)):
@@ -551,7 +571,7 @@ def run_gpu(args):
             stream.wait_event(ev_out[b])
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        last = ohost[(args.steps - 1) % nbuf][0]
+        last = ohost[(args.steps - 1) % nbuf][1][0]
         e2e_ms = e0.elapsed_time(e1) / args.steps
     else:  # L2 flushed before each step (untimed); copies and kernels in one stream
         e2e_spans = []
@@ -560,15 +580,13 @@ def run_gpu(args):
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
             a0.record(stream)
-            for hb, db in zip(host, sets[0]):
-                db.copy_(hb, non_blocking=True)
-            step(*sets[0], o=osets[0][0], op=osets[0][1] if has_prefill else None)
-            for hb, db in zip(ohost[0], osets[0]):
-                hb.copy_(db, non_blocking=True)
+            dsets[0][0].copy_(hbuf, non_blocking=True)
+            run_set(0)
+            ohost[0][0].copy_(osets[0][0], non_blocking=True)
             a1.record(stream)
             e2e_spans.append((a0, a1))
         torch.cuda.synchronize(dev)
-        last = ohost[0][0]
+        last = ohost[0][1][0]
         e2e_ms = float(sum(x.elapsed_time(y) for x, y in e2e_spans)) / args.steps
     if not torch.equal(last, out.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident run")
