@@ -224,6 +224,11 @@ PKV_API size_t pkv_paged_attention_noalloc_max_scratch(void);
  *   out             device, bf16 [num_q_tokens][num_q_heads][head_dim]
  * head_dim 64 or 128 and a bf16 pool (FP8 pools: PKV_ERR_UNSUPPORTED); the
  * group size num_q_heads/num_kv_heads must divide 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
+ * Device data: a sequence whose rows fall outside 0 .. num_q_tokens-1, whose
+ * chunk is longer than max_q_len or than L_s, or whose L_s exceeds
+ * max_blocks_per_seq pages is skipped (its rows are not written) and
+ * recorded for pkv_get_device_error (PKV_ERR_DEVICE_BOUNDS); a page id out of
+ * range is recorded and read as zeros.
  */
 PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
                              const void *k_pool, const void *v_pool,

@@ -293,7 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int s = group / max_pairs, pair = group - s * max_pairs;
   const int q0 = __ldg(p.cu_seqlens_q + s);
-  const int C = __ldg(p.cu_seqlens_q + s + 1) - q0;
+  const int q1 = __ldg(p.cu_seqlens_q + s + 1);
+  // the chunk's rows must lie inside q / out and inside the grid's tiles
+  // (max_q_len): otherwise the sequence is recorded and skipped
+  if (q0 < 0 || q1 < q0 || q1 > p.num_q_tokens ||
+      int64_t(q1 - q0) * G > int64_t(p.tiles_per_seq) * kM) {
+    if (threadIdx.x == 0 && pair == 0) record_error(p.err, kDevBadPage);
+    return;
+  }
+  const int C = q1 - q0;
   const int tokA = pair * kTiles * TQ;            // first chunk token of tile 0
   if (C <= 0 || tokA >= C) return;
   const int L = __ldg(p.context_lens + s);

@@ -137,6 +137,41 @@ def test_bad_page_id_reported():
     assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_BOUNDS
 
 
+def test_rows_outside_q_are_reported_and_not_written():
+    # the last chunk's end points past num_q_tokens: that sequence is skipped
+    # and recorded, the others are computed, nothing lands past the output
+    w = W.make_mixed("prefill_bad_cu", 6262, [20], [30, 0, 200], [40, 5, 100], 16, 4, 128, 32)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp)
+    T, Hq, D = d["q_prefill"].shape
+    big = torch.full((T + 64, Hq, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    cu = d["cu_seqlens_q"].clone()
+    cu[-1] = T + 40
+    pkv.paged_prefill(d["q_prefill"], cu, kp, vp, d["prefill_block_tables"],
+                      d["prefill_context_lens"], 200, w.scale, out=big[:T])
+    assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_BOUNDS
+    assert torch.all(big[int(w.cu_seqlens_q()[2]):].float() == 7.0)
+    _check(w, big[:T], seqs=[0, 1])
+
+
+def test_chunk_longer_than_max_q_len_is_reported_and_not_written():
+    # max_q_len 32 at G = 4 sizes the grid for one 32-token tile per sequence:
+    # the 40- and 100-token chunks are skipped and recorded, the 5-token one runs
+    w = W.make_mixed("prefill_short_max_q", 6363, [20], [30, 0, 200], [40, 5, 100], 16, 4, 128,
+                     32)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp)
+    out = torch.full_like(d["q_prefill"], 7.0)
+    pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp, d["prefill_block_tables"],
+                      d["prefill_context_lens"], 32, w.scale, out=out)
+    assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_BOUNDS
+    cu = w.cu_seqlens_q()
+    assert torch.all(out[cu[0]:cu[1]].float() == 7.0) and torch.all(out[cu[2]:cu[3]].float() == 7.0)
+    _check(w, out, seqs=[1])
+
+
 def test_full_size_mixed_step_sampled():
     w = W.config(5)
     d = device_step_inputs(w)
