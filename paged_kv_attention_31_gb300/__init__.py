@@ -187,6 +187,21 @@ def pool_desc(k_pool: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0,
                     _scales_ptr(v_scales, hkv))
 
 
+def _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, rows):
+    """The kernels see only pointers: q / out, both pools and the per-sequence
+    tables must have the sizes the call implies (`rows` sequences)."""
+    if v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("k_pool and v_pool differ")
+    if q.shape[2] != desc.head_dim:
+        raise ValueError(f"q head_dim {q.shape[2]} differs from the pool's {desc.head_dim}")
+    if out.shape != q.shape or out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16 with q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] < rows:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    if context_lens.dim() != 1 or context_lens.shape[0] < rows:
+        raise ValueError("context_lens must hold one length per sequence")
+
+
 def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale=1.0, v_scale=1.0,
               stream=None, k_scales=None, v_scales=None) -> None:
     """Write new tokens' K/V rows ([T, Hkv, D] bf16) to their pool slots."""
@@ -240,6 +255,7 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_l
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
     if workspace is None:
         nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool,
                                                 partition_tokens, k_scale, v_scale)
@@ -277,6 +293,7 @@ def paged_attention_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
     if workspace is None:
         nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool, partition_tokens,
                                                 k_scale, v_scale)
@@ -304,6 +321,7 @@ def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_c
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
     _check(lib().pkv_paged_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
                                              ctypes.byref(desc), _ptr(block_tables),
                                              int(block_tables.shape[1]), _ptr(context_lens),
@@ -326,6 +344,9 @@ def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens, m
     n = int(context_lens.shape[0])
     if out is None:
         out = torch.empty_like(q)
+    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, n)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] != n + 1:
+        raise ValueError("cu_seqlens_q must be [num_seqs + 1]")
     _check(lib().pkv_paged_prefill(_ptr(q), _ptr(cu_seqlens_q), _ptr(k_pool), _ptr(v_pool),
                                    ctypes.byref(desc), _ptr(block_tables),
                                    int(block_tables.shape[1]), _ptr(context_lens), n, int(Hq),
