@@ -624,7 +624,8 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 kv, bf16 q/out",
         "data": "synthetic", "config": _config(w, args),
-        "seq_steps_per_s": world * B / (ms * 1e-3),
+        # every sequence of the iteration advances one step (prefill chunks too)
+        "seq_steps_per_s": world * (B + w.num_prefill) / (ms * 1e-3),
         "frac_of_hbm_peak": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
@@ -650,7 +651,10 @@ def run_gpu(args):
         line["logical_kv_gbs"] = (w.decode_kv_bytes(unique=False) + (attn_bytes - w.decode_kv_bytes())) \
             / (attn_ms * 1e-3) / 1e9
     if has_prefill:
-        line["tokens_per_s"] = world * (B + int(np.sum(w.prefill_chunk_lens))) / (ms * 1e-3)
+        tokens = B + int(np.sum(w.prefill_chunk_lens))
+        line["sequences_per_iteration"] = B + w.num_prefill
+        line["tokens_per_iteration"] = tokens
+        line["tokens_per_s"] = world * tokens / (ms * 1e-3)
         flops = w.prefill_flops()
         tpeak = float(peaks["bf16_tflops"])
         tflops = flops / (prefill_ms * 1e-3) / 1e12
