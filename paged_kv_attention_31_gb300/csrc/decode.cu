@@ -209,14 +209,41 @@ __device__ void plan_items(const DecodeParams& p) {
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int pos = 0;
-    for (int b = nb - 1; b >= 0; --b) {  // longest items first
-      offs[b] = pos;
-      pos += hist[b];
+  // offs[b] = items in the buckets above b (longest items first): an
+  // exclusive scan over the buckets in decreasing order, two buckets per
+  // thread (nb <= 2 * blockDim.x)
+  {
+    __shared__ int warp_sum[32];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int r0 = 2 * t, r1 = 2 * t + 1;  // positions in decreasing bucket order
+    const int v0 = r0 < nb ? hist[nb - 1 - r0] : 0;
+    const int v1 = r1 < nb ? hist[nb - 1 - r1] : 0;
+    int incl = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    p.counters[0] = pos;
-    p.counters[1] = 0;
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int nw = (blockDim.x + 31) >> 5;
+      int w = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nw) warp_sum[lane] = w;  // inclusive totals of warps 0 .. lane
+      if (lane == nw - 1) {
+        p.counters[0] = w;
+        p.counters[1] = 0;
+      }
+    }
+    __syncthreads();
+    const int before = (wid > 0 ? warp_sum[wid - 1] : 0) + incl - (v0 + v1);
+    if (r0 < nb) offs[nb - 1 - r0] = before;
+    if (r1 < nb) offs[nb - 1 - r1] = before + v0;
   }
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
