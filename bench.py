@@ -343,7 +343,9 @@ def _config(w, args):
          "l2": args.l2_note,
          "parallelism": f"replicas x{args.gpus}",
          "launch": "cuda_graph_replay" if args.graph else "eager",
-         "step_calls": ("pkv_paged_attention_append" if args.fused else
+         "step_calls": ("pkv_kv_append, then pkv_paged_attention (high-priority stream) "
+                        "beside pkv_paged_prefill" if getattr(args, "concurrent", False) else
+                        "pkv_paged_attention_append" if args.fused else
                         "pkv_kv_append + pkv_paged_attention")}
     if w.num_prefill:
         c["prefill_chunks"] = [int(x) for x in w.prefill_chunk_lens]
@@ -398,10 +400,32 @@ def run_gpu(args):
         out_p = torch.empty_like(d["q_prefill"])
         max_q = int(w.prefill_chunk_lens.max())
     stream = torch.cuda.current_stream(dev)
+    # The mixed step's two attention calls are independent once the step's
+    # rows are appended: by default the decode call runs on a high-priority
+    # stream beside the prefill, so each fills the SMs the other's tail leaves
+    # idle (the append then is its own call, ahead of both).
+    args.concurrent = has_prefill and not args.mixed_serial
+    if args.concurrent:
+        args.fused = False
+        hi_s = torch.cuda.Stream(dev, priority=-1)
+        ev_app, ev_dec = torch.cuda.Event(), torch.cuda.Event()
 
     def step(q, k_new, v_new, slots, bt, cl, qp=None, cu=None, pbt=None, pcl=None, ev=None,
              o=None, op=None, decode_only=False):
         o = out if o is None else o
+        if args.concurrent and ev is None and not decode_only:
+            m = torch.cuda.current_stream(dev)  # the capture stream under --graph
+            pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
+            ev_app.record(m)
+            hi_s.wait_event(ev_app)
+            pkv.paged_prefill(qp, cu, kp, vp, pbt, pcl, max_q, w.scale,
+                              out=out_p if op is None else op)
+            pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
+                                workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
+                                partition_tokens=args.partition, stream=hi_s)
+            ev_dec.record(hi_s)
+            m.wait_event(ev_dec)
+            return
         if args.fused:  # the append runs inside the attention call's planning launch
             if ev is not None:
                 ev[0].record(stream)
@@ -409,7 +433,8 @@ def run_gpu(args):
                                        w.scale, out=o, workspace=ws, k_scale=w.k_scale,
                                        v_scale=w.v_scale, partition_tokens=args.partition)
         else:
-            pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
+            if not decode_only:  # a decode-only pass times the attention call alone
+                pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
             if ev is not None:
                 ev[0].record(stream)
             pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
@@ -688,6 +713,10 @@ def main(argv=None):
     ap.add_argument("--separate-append", dest="fused", action="store_false",
                     help="two calls per decode step (pkv_kv_append, then pkv_paged_attention) "
                          "instead of pkv_paged_attention_append")
+    ap.add_argument("--mixed-serial", action="store_true",
+                    help="mixed workload: the decode call, then the prefill call, on one stream "
+                         "(default: one append of every new row, then the decode call on a "
+                         "high-priority stream beside the prefill)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the step in a CUDA graph and time its replays")
     ap.add_argument("--num-seqs", type=int, default=None,
