@@ -50,9 +50,11 @@ def test_default_decode_line():
     assert b["ms_per_launch"] > 0 and abs(b["achieved"] / d["roofline"]["peak"] - b["frac"]) < 1e-9
 
 
-def test_mixed_step_line_reports_the_tensor_roofline():
-    d = _run("--workload", "5", "--no-cpu-baseline")
+@pytest.mark.parametrize("schedule", [(), ("--mixed-serial",)])
+def test_mixed_step_line_reports_the_tensor_roofline(schedule):
+    d = _run("--workload", "5", "--no-cpu-baseline", *schedule)
     _common(d)
+    assert ("beside" in d["config"]["step_calls"]) == (not schedule)
     assert d["roofline"]["bound"] == "tensor" and d["roofline"]["unit"] == "TFLOP/s"
     assert d["decode_roofline"]["bound"] == "hbm"
     assert d["decode_roofline"]["back_to_back"]["ms_per_launch"] > 0
