@@ -173,3 +173,64 @@ def test_the_attention_oracle_itself_passes_these_pins(monkeypatch):
                                     _page_off_by_one, _fp8_scales_swapped])
 def test_a_planted_attention_mistake_fails_a_pin(monkeypatch, mutant):
     assert _failing_attention_pins(monkeypatch, mutant), f"{mutant.__name__} passed every pin"
+
+
+# ---- prefill and append oracles -------------------------------------------------
+_real_prefill = oracle.paged_prefill
+_real_append = oracle.kv_append
+
+
+def _chunk_lens(cu):
+    cu = np.asarray(cu)
+    return cu[1:] - cu[:-1]
+
+
+def _prefill_one_key_more(q, cu, kp, vp, bt, cl, scale, *a, **k):
+    # causal window one key too wide (key <= position + 1)
+    return _real_prefill(q, cu, kp, vp, bt, (np.asarray(cl) + 1).astype(np.int32), scale, *a, **k)
+
+
+def _prefill_own_key_masked(q, cu, kp, vp, bt, cl, scale, *a, **k):
+    # strict mask (key < position): emulated by positions one lower wherever
+    # the sequence has a prior token to attend instead
+    cl = np.asarray(cl)
+    return _real_prefill(q, cu, kp, vp, bt, np.maximum(cl - 1, _chunk_lens(cu)).astype(np.int32),
+                         scale, *a, **k)
+
+
+def _append_slot_plus_one(k_new, v_new, slots, kp, vp, *a, **k):
+    return _real_append(k_new, v_new, (np.asarray(slots) + 1).astype(np.int64), kp, vp, *a, **k)
+
+
+def _failing_calls(monkeypatch, attr, impl, calls):
+    monkeypatch.setattr(oracle, attr, impl)
+    failed = []
+    for name, a in calls:
+        try:
+            getattr(attn_pins, name)(*a)
+        except (AssertionError, ValueError, RuntimeError):
+            failed.append(name)
+    return failed
+
+
+_PREFILL_PINS = [(n, ()) for n in ("test_prefill_matches_masked_dense_sdpa",
+                                   "test_prefill_chunk_of_one_equals_decode",
+                                   "test_prefill_row_equals_truncated_decode")]
+_APPEND_PINS = [(n, ()) for n in ("test_kv_append_scatter_read_back",
+                                  "test_kv_append_out_of_pool_counted_and_skipped",
+                                  "test_kv_append_fp8_matches_torch_quantisation",
+                                  "test_kv_append_fp8_per_head_scales_match_torch")]
+
+
+def test_prefill_and_append_oracles_pass_these_pins(monkeypatch):
+    assert _failing_calls(monkeypatch, "paged_prefill", _real_prefill, _PREFILL_PINS) == []
+    assert _failing_calls(monkeypatch, "kv_append", _real_append, _APPEND_PINS) == []
+
+
+@pytest.mark.parametrize("mutant", [_prefill_one_key_more, _prefill_own_key_masked])
+def test_a_planted_prefill_mistake_fails_a_pin(monkeypatch, mutant):
+    assert _failing_calls(monkeypatch, "paged_prefill", mutant, _PREFILL_PINS)
+
+
+def test_a_planted_append_mistake_fails_a_pin(monkeypatch):
+    assert _failing_calls(monkeypatch, "kv_append", _append_slot_plus_one, _APPEND_PINS)
