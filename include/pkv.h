@@ -32,11 +32,12 @@
  *    (never dereferenced) and recorded in a sticky per-device error word that
  *    pkv_get_device_error returns.  Kernels never trap and every wait in them
  *    is bounded; a wait that runs out is recorded the same way.
- *  - Host threads: calls from several host threads are safe once each
- *    device has seen its first call; that first call (which looks up the
- *    device's SM count and sets kernel attributes, cached per device) should
- *    be made from one thread.  A pkv_cache_* handle is not synchronised:
- *    use each one from one thread at a time.
+ *  - Host threads: per-device set-up (the SM count, kernel shared-memory
+ *    attributes) is cached on first use in variables that are not
+ *    synchronised between host threads.  Make the calls that may set a
+ *    device up -- its first call, and its first decode with a longer split
+ *    partition -- from one thread, or serialise them.  A pkv_cache_* handle
+ *    is not synchronised either: use each from one thread at a time.
  *
  * Data layout
  *  - KV pool: k_pool, v_pool = [num_blocks][num_kv_heads][block_size][head_dim],
