@@ -32,12 +32,11 @@
  *    (never dereferenced) and recorded in a sticky per-device error word that
  *    pkv_get_device_error returns.  Kernels never trap and every wait in them
  *    is bounded; a wait that runs out is recorded the same way.
- *  - Host threads: per-device set-up (the SM count, kernel shared-memory
- *    attributes) is cached on first use in variables that are not
- *    synchronised between host threads.  Make the calls that may set a
- *    device up -- its first call, and its first decode with a longer split
- *    partition -- from one thread, or serialise them.  A pkv_cache_* handle
- *    is not synchronised either: use each from one thread at a time.
+ *  - Host threads: the entry points may be called from several host threads
+ *    at once (each on its own stream and buffers); the per-device set-up done
+ *    on first use (SM count, kernel shared-memory attributes) is guarded.
+ *    A pkv_cache_* handle is not synchronised: use each from one thread at a
+ *    time.
  *
  * Data layout
  *  - KV pool: k_pool, v_pool = [num_blocks][num_kv_heads][block_size][head_dim],

@@ -640,18 +640,17 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t stream) 
   const int max_pages = (p.partition + p.block_size - 1) / p.block_size + 1;
   const int smem = align_up(C::OFF_PG + 4 * max_pages, 16);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  // per-device cache of the attribute / occupancy setup (smem varies with
-  // the partition, so occupancy is queried for the size at hand)
-  static int configured_smem[64] = {0};
+  // the shared-memory ceiling is raised once per device; smem varies with
+  // the partition, so occupancy is queried for the size at hand
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured_smem[dev] < smem) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = 227 * 1024;
-  }
+  e = once_per_device(configured, dev, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NTHR, smem);
   if (e != cudaSuccess) return e;

@@ -483,16 +483,15 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
   const int max_pages = (p.partition + p.block_size - 1) / p.block_size + 1;
   const int smem = C::OFF_PG + 4 * max_pages + 16 + 1024;  // + alignment slack
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  e = once_per_device(configured, dev, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, smem);
   if (e != cudaSuccess) return e;

@@ -26,18 +26,22 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<bool> g_scratch_ready[kMaxDevices];
 
 // Per-device set-up: resolve the device address of the scratch array with
 // that device current.  Done once per device, on its first call.
 pkv_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
+  const cudaError_t e = pkv::once_per_device(g_scratch_ready, dev, [&]() -> cudaError_t {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
-      return PKV_ERR_CUDA;
+    const cudaError_t r = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (r != cudaSuccess) return r;
+    if (!ptr) return cudaErrorInvalidSymbol;
     g_scratch_addr[dev] = ptr;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
   *out = g_scratch_addr[dev];
   return PKV_OK;
 }

@@ -17,24 +17,26 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int num_sms = 0;
   int32_t* err = nullptr;
-  bool ready = false;
 };
 DeviceInfo g_dev[kMaxDevices];
+std::atomic<bool> g_dev_ready[kMaxDevices];
 
 pkv_status device_info(DeviceInfo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
+  const cudaError_t e = pkv::once_per_device(g_dev_ready, dev, [&]() -> cudaError_t {
     int sms = 0;
     void* addr = nullptr;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    if (cudaGetSymbolAddress(&addr, g_pkv_device_error) != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r != cudaSuccess) return r;
+    r = cudaGetSymbolAddress(&addr, g_pkv_device_error);
+    if (r != cudaSuccess) return r;
     d.num_sms = sms;
     d.err = static_cast<int32_t*>(addr);
-    d.ready = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
   *out = &d;
   return PKV_OK;
 }

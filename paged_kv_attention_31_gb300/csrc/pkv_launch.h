@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <utility>
 
 namespace pkv {
@@ -28,6 +30,24 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Per-device one-time host set-up (kernel attributes, cached lookups) that
+// concurrent host threads may reach together: `setup` runs under one lock
+// until it first succeeds for the device; `done[dev]` then publishes its
+// results (release / acquire) and later calls skip the lock.
+inline std::mutex& setup_mutex() {
+  static std::mutex m;
+  return m;
+}
+template <typename F>
+cudaError_t once_per_device(std::atomic<bool>* done, int dev, F&& setup) {
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(setup_mutex());
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = setup();
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
 }
 
 struct AppendParams {

@@ -660,17 +660,16 @@ cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const v
   if (!make_map_4d(&tv, kBf16, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
                    Hkv * P * D * E, 64, uint32_t(P), 1, 1))
     return cudaErrorInvalidValue;
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  e = once_per_device(configured, dev, [&] {
+    return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   // one CTA per pair of 128-row query tiles of one kv head
   const int64_t ctas =
       int64_t((p.tiles_per_seq + kTiles - 1) / kTiles) * p.num_kv_heads * p.num_seqs;
