@@ -6,15 +6,23 @@ heads, head_dim 128, block size 64, context lengths U[128, 4096], bf16 KV,
 tokens + paged decode attention over the whole batch, in one call
 (pkv_paged_attention_append: planning and append in one launch, split-K
 decode, merge); --separate-append makes it two calls (pkv_kv_append, then
-pkv_paged_attention).  --workload selects another configuration (1..5);
-configuration 5 adds the chunked-prefill call to the step.
+pkv_paged_attention).  --workload selects another configuration (1..5).
+Configuration 5 is a mixed iteration: one pkv_kv_append of every new row,
+then pkv_paged_prefill on the step's stream beside pkv_paged_attention on a
+high-priority stream (--mixed-serial: the fused decode call, then the
+prefill, on one stream).
 
 Prints ONE JSON line.  `value` = algorithmic bytes of the step / device time
-per step (K/V bytes streamed dominate: 2 * head_dim * element size per token
-and kv head, plus q, out, block-table entries and the appended rows).  `e2e` is the
-same metric through the public API with inputs copied from pinned host memory
-and the output copied back inside the timed region.  --impl reference times
-the fp64 CPU oracle on a bounded sample of the same workload.
+per step, the steps running back to back with no event inside them (K/V
+bytes streamed dominate: 2 * head_dim * element size per token and kv head,
+plus q, out, block-table entries and the appended rows).  `roofline` is the
+dominant call's own rate from a second pass with CUDA events around each
+call, and `roofline.back_to_back` the same call timed with its launches
+chained.  A workload whose K/V fits in the L2 is flushed before every step.
+`e2e` is the same metric through the public API with inputs copied from
+pinned host memory and the output copied back inside the timed region.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU
 (nothing in the step shards across GPUs); value = all ranks' bytes / the
