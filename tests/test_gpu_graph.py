@@ -1,8 +1,8 @@
 """The decode step (kv_append + paged attention) captured in a CUDA graph and
 replayed gives bit-identical results to eager launches: every call is
 stream-ordered and synchronises nothing, so a batch-size bucket can be
-captured once and replayed each step (the pages' CUDA-graph advice,
-"CUDA Graph优化", §8.1)."""
+captured once and replayed each step ("TensorRT-LLM框架解析与高性能推理优化实践"
+§8.1, "CUDA Graph优化")."""
 import pytest
 import torch
 
