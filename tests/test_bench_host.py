@@ -59,3 +59,23 @@ def test_reference_arm_prints_one_json_line():
     assert rec["impl"] == "reference" and rec["unit"] == "GB/s" and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["config"]["workload"].startswith("tiny_decode")
+
+
+def test_l2_flush_only_where_the_working_set_fits_in_cache():
+    # the tiny decode workload (0.14 MB of K/V) is flushed before every step;
+    # the others stream far more than twice the L2 and are not
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    for i, flush in ((1, True), (2, False), (3, False), (4, False), (5, False)):
+        w = W.config(i)
+        args = argparse.Namespace(gpus=1, partition=0, graph=False, fused=True, concurrent=False)
+        l2 = bench._l2_plan(w, args)
+        assert l2 > 0 and args.flush is flush, i
+        assert ("flushed" in args.l2_note) is flush
+        c = bench._config(w, args)
+        assert c["workload"] == w.name and c["l2"] == args.l2_note
+        assert c["step_calls"] == "pkv_paged_attention_append"
+    args.concurrent = True
+    assert "beside pkv_paged_prefill" in bench._config(W.config(5), args)["step_calls"]
