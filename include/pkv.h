@@ -251,6 +251,21 @@ PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
  */
 PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
 
+/*
+ * pkv_self_test_bounded_wait -- a check of the kernels' failure path on the
+ * current device: one small kernel waits, with a limit of limit_cycles SM
+ * clock cycles (0 < limit_cycles <= 2e9), on a barrier that nothing arrives
+ * at.  The wait must give up, record PKV_ERR_DEVICE_TIMEOUT in the sticky
+ * error word (read it with pkv_get_device_error) and raise the kernel's
+ * abort flag, after which a second wait returns at once; the kernel then
+ * ends normally and the context stays usable.
+ *   out   device, int32 [5], 4-byte aligned: first wait's result (expect 0),
+ *         second wait's result (0), abort flag (1), first wait lasted at
+ *         least limit_cycles (1), second lasted less than limit_cycles / 4 (1).
+ * Enqueued on `stream`; PKV_ERR_INVALID_ARG for a bad pointer or limit.
+ */
+PKV_API pkv_status pkv_self_test_bounded_wait(int64_t limit_cycles, int32_t *out, void *stream);
+
 /* Text of the last CUDA error a call of this library met on the calling
  * thread (explains PKV_ERR_CUDA; "no error" if none).  Never NULL. */
 PKV_API const char *pkv_last_cuda_error(void);

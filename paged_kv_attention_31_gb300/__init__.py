@@ -121,6 +121,8 @@ def lib():
             L.pkv_cache_block_tables.argtypes = [vp, vp, i32, vp, vp]
             L.pkv_get_device_error.restype = i32
             L.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
+            L.pkv_self_test_bounded_wait.restype = i32
+            L.pkv_self_test_bounded_wait.argtypes = [i64, vp, vp]
             L.pkv_last_cuda_error.restype = ctypes.c_char_p
             L.pkv_last_cuda_error.argtypes = []
             L.pkv_status_string.restype = ctypes.c_char_p
@@ -462,6 +464,15 @@ class KVCacheManager:
         _check(lib().pkv_cache_block_tables(self._h, _np_ptr(ids), n, _np_ptr(tab),
                                             _np_ptr(lens)), "pkv_cache_block_tables")
         return tab, lens
+
+
+def self_test_bounded_wait(limit_cycles: int = 1_000_000, stream=None) -> list:
+    """Run the failure-path check (pkv_self_test_bounded_wait) and return its
+    five results; the device error word then holds PKV_ERR_DEVICE_TIMEOUT."""
+    out = torch.full((5,), -1, dtype=torch.int32, device="cuda")
+    _check(lib().pkv_self_test_bounded_wait(int(limit_cycles), _ptr(out), _stream(stream)),
+           "pkv_self_test_bounded_wait")
+    return [int(x) for x in out.cpu()]
 
 
 def get_device_error(stream=None) -> int:

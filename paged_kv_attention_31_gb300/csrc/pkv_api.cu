@@ -100,6 +100,34 @@ pkv_status validate_partition(int32_t partition, int block_size) {
   return PKV_OK;
 }
 
+// Self-test of the failure path: a wait on a barrier that nothing arrives at
+// must give up after `limit` cycles, record PKV_ERR_DEVICE_TIMEOUT and raise
+// the abort flag, after which a second wait returns at once.  out[0..4]:
+// first wait's result (0), second wait's result (0), abort flag (1), first
+// wait took >= limit cycles (1), second took < limit / 4 cycles (1).
+__global__ void self_test_wait_kernel(int32_t* err, long long limit, int32_t* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    pkv::mbar_init(&bar, 1);
+    abort_flag = 0;
+    pkv::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  volatile int* flag = &abort_flag;
+  const long long t0 = clock64();
+  const bool first = pkv::mbar_wait_bounded(&bar, 0, err, flag, limit);
+  const long long t1 = clock64();
+  const bool second = pkv::mbar_wait_bounded(&bar, 0, err, flag, limit);
+  const long long t2 = clock64();
+  out[0] = first ? 1 : 0;
+  out[1] = second ? 1 : 0;
+  out[2] = *flag;
+  out[3] = (t1 - t0) >= limit ? 1 : 0;
+  out[4] = (t2 - t1) < limit / 4 ? 1 : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -388,6 +416,18 @@ pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const v
   p.q_mult = scale * 1.4426950408889634f;
   return from_cuda(
       pkv::launch_prefill(p, k_pool, v_pool, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_self_test_bounded_wait(int64_t limit_cycles, int32_t* out, void* stream) {
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 3) || limit_cycles <= 0 ||
+      limit_cycles > pkv::kWaitLimitCycles)
+    return PKV_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  self_test_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->err, limit_cycles,
+                                                                        out);
+  return from_cuda(cudaGetLastError());
 }
 
 pkv_status pkv_get_device_error(int32_t* code, void* stream) {

@@ -80,12 +80,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // so a kernel whose copies never land finishes in about one wait limit
 // instead of one limit per wait.  Returns false when it did not see the phase.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* err,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag,
+                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       record_error(err, kDevTimeout);
       *abort_flag = 1;
       return false;

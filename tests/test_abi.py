@@ -122,3 +122,11 @@ def test_workspace_size_is_positive(lib):
     d = _desc()
     assert lib.pkv_paged_attention_workspace_size(4, 8, 1000, 0, ctypes.byref(d)) > 0
     assert lib.pkv_paged_attention_workspace_size(4, 8, 1000, 24, ctypes.byref(d)) == 0
+
+
+def test_self_test_validation_before_any_cuda_call(lib):
+    out = ctypes.c_void_p(256)
+    assert lib.pkv_self_test_bounded_wait(1000, None, None) == 1          # no output buffer
+    assert lib.pkv_self_test_bounded_wait(0, out, None) == 1              # limit must be > 0
+    assert lib.pkv_self_test_bounded_wait(3_000_000_000, out, None) == 1  # above the kernels' own
+    assert lib.pkv_self_test_bounded_wait(1000, ctypes.c_void_p(258), None) == 1  # misaligned
