@@ -75,7 +75,7 @@ def lib():
                                                     i32, i32, p, i32, p, i32, p, p,
                                                     i32, f64, p]
             L.pkvo_paged_prefill.restype = i32
-            L.pkvo_paged_prefill.argtypes = [p, p, p, p, i32, f32, f32, i64, i32, i32,
+            L.pkvo_paged_prefill.argtypes = [p, p, p, p, i32, f32, f32, p, p, i64, i32, i32,
                                              i32, p, i32, p, i32, i32, f64, p]
             _lib = L
     return _lib
@@ -216,8 +216,10 @@ def paged_attention_rows(q, k_pool, v_pool, block_tables, context_lens, scale,
 
 
 def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens,
-                  scale, kv_dtype="bf16", k_scale=1.0, v_scale=1.0) -> np.ndarray:
-    """fp64 out [T_p, Hq, D]: causal attention of packed chunk tokens."""
+                  scale, kv_dtype="bf16", k_scale=1.0, v_scale=1.0, k_scales=None,
+                  v_scales=None) -> np.ndarray:
+    """fp64 out [T_p, Hq, D]: causal attention of packed chunk tokens (FP8
+    pools: per-tensor scales, or per-kv-head k_scales / v_scales)."""
     _check_pool(k_pool, kv_dtype)
     q = np.ascontiguousarray(q, dtype=np.uint16)
     cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
@@ -228,9 +230,11 @@ def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens,
     n = cl.shape[0]
     assert cu.shape == (n + 1,) and int(cu[-1]) == T
     out = np.zeros((T, Hq, D), dtype=np.float64)
+    ka, kptr = _scales(k_scales, hkv)
+    va, vptr = _scales(v_scales, hkv)
     bad = lib().pkvo_paged_prefill(_ptr(q), _ptr(cu), _ptr(k_pool), _ptr(v_pool),
-                                   _dtype_code(kv_dtype), k_scale, v_scale, nb, hkv, P,
-                                   D, _ptr(bt), bt.shape[1], _ptr(cl), n, Hq,
+                                   _dtype_code(kv_dtype), k_scale, v_scale, kptr, vptr, nb,
+                                   hkv, P, D, _ptr(bt), bt.shape[1], _ptr(cl), n, Hq,
                                    float(scale), _ptr(out))
     if bad:
         raise ValueError(f"{bad} rows reference pages outside the pool")

@@ -266,10 +266,12 @@ int pkvo_paged_attention_rows(const uint16_t *q, const void *k_pool,
 /* q [T_p][Hq][D] packed: sequence s owns rows cu_seqlens_q[s] ..
  * cu_seqlens_q[s+1]-1, C_s of them; context_lens[s] = L_s counts the chunk.
  * Row i of sequence s attends to keys 0 .. L_s - C_s + i (causal over pages).
- * out [T_p][Hq][D] fp64. */
+ * FP8 pools: scales per kv head when k_scales / v_scales are given, as in
+ * the decode.  out [T_p][Hq][D] fp64. */
 int pkvo_paged_prefill(const uint16_t *q, const int32_t *cu_seqlens_q,
                        const void *k_pool, const void *v_pool, int kv_dtype,
-                       float k_scale, float v_scale, int64_t num_blocks, int Hkv,
+                       float k_scale, float v_scale, const float *k_scales,
+                       const float *v_scales, int64_t num_blocks, int Hkv,
                        int P, int D, const int32_t *block_tables, int max_blocks,
                        const int32_t *context_lens, int n, int Hq, double scale,
                        double *out)
@@ -283,7 +285,8 @@ int pkvo_paged_prefill(const uint16_t *q, const int32_t *cu_seqlens_q,
             int visible = L - C + i + 1;
             for (int a = 0; a < Hq; a++)
                 bad += pkvo_attention_one(q + (row * Hq + a) * D, k_pool, v_pool,
-                                          kv_dtype, k_scale, v_scale, num_blocks,
+                                          kv_dtype, k_scales ? k_scales[a / G] : k_scale,
+                                          v_scales ? v_scales[a / G] : v_scale, num_blocks,
                                           Hkv, P, D, a / G,
                                           block_tables + (int64_t)s * max_blocks,
                                           visible, scale,

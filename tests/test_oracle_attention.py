@@ -222,6 +222,63 @@ def test_prefill_row_equals_truncated_decode():
         assert np.array_equal(out[i], want[0])
 
 
+def _fp8_prefill_case(seed, priors, chunks, Hq, Hkv, D, P):
+    """Pools of random E4M3 codes (NaN codes replaced) and bf16 q."""
+    rng = np.random.default_rng(seed)
+    lens = [p + c for p, c in zip(priors, chunks)]
+    codes = lambda n: rng.integers(0, 256, (n, Hkv, D)).astype(np.uint8)
+    Kc = [codes(L) for L in lens]
+    Vc = [codes(L) for L in lens]
+    for x in Kc + Vc:                              # no NaN codes
+        x[(x & 0x7F) == 0x7F] = 0x7E
+    nb = sum((L + P - 1) // P for L in lens) + 3
+    kp, bt = paginate(Kc, P, nb, np.random.default_rng(seed + 1), np.uint8)
+    vp, _ = paginate(Vc, P, nb, np.random.default_rng(seed + 1), np.uint8)
+    cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = _rand_bf16(rng, (int(cu[-1]), Hq, D), 0.05)
+    return q, cu, Kc, Vc, kp, vp, bt, np.array(lens, np.int32)
+
+
+@pytest.mark.parametrize("per_head", [False, True])
+def test_prefill_fp8_matches_masked_dense_dequantised(per_head):
+    # the chunked prefill over an FP8 pool: torch's E4M3 decoding of the same
+    # codes times the scales (per tensor, or per kv head), dense masked SDPA
+    priors, chunks = [0, 6, 13], [9, 2, 5]
+    Hq, Hkv, D, P = 6, 2, 16, 4
+    q, cu, Kc, Vc, kp, vp, bt, cl = _fp8_prefill_case(23, priors, chunks, Hq, Hkv, D, P)
+    if per_head:
+        ks = np.array([0.011, 0.0045], np.float32)
+        vs = np.array([0.02, 0.037], np.float32)
+        out = oracle.paged_prefill(q, cu, kp, vp, bt, cl, 0.25, "fp8_e4m3", 5.0, 5.0,
+                                   k_scales=ks, v_scales=vs)
+    else:
+        ks = np.full(Hkv, 0.011, np.float32)
+        vs = np.full(Hkv, 0.02, np.float32)
+        out = oracle.paged_prefill(q, cu, kp, vp, bt, cl, 0.25, "fp8_e4m3", 0.011, 0.02)
+    deq = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for s in range(3):
+        L, C = int(cl[s]), chunks[s]
+        rows = slice(cu[s], cu[s + 1])
+        mask = np.arange(L)[None, :] <= (L - C + np.arange(C))[:, None]
+        K = deq(Kc[s]) * ks.astype(np.float64)[None, :, None]
+        V = deq(Vc[s]) * vs.astype(np.float64)[None, :, None]
+        ref = dense_attention(bf16_to_f64(q[rows]).transpose(1, 0, 2), K.transpose(1, 0, 2),
+                              V.transpose(1, 0, 2), 0.25, mask=mask)
+        np.testing.assert_allclose(out[rows], ref.transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+def test_prefill_fp8_row_equals_truncated_decode_with_head_scales():
+    q, cu, Kc, Vc, kp, vp, bt, cl = _fp8_prefill_case(24, [5], [11], 4, 2, 8, 4)
+    ks = np.array([0.013, 0.006], np.float32)
+    vs = np.array([0.03, 0.011], np.float32)
+    out = oracle.paged_prefill(q, cu, kp, vp, bt, cl, 0.5, "fp8_e4m3", k_scales=ks, v_scales=vs)
+    for i in range(11):
+        trunc = np.array([5 + i + 1], np.int32)
+        want = oracle.paged_attention(q[i:i + 1], kp, vp, bt, trunc, 0.5, "fp8_e4m3",
+                                      k_scales=ks, v_scales=vs)
+        assert np.array_equal(out[i], want[0])
+
+
 # ---- kv_append ---------------------------------------------------------------
 def _slots_view(pool):
     """[num_blocks*P, Hkv, D] view of a pool: row = page*P + offset."""

@@ -198,6 +198,27 @@ def _prefill_own_key_masked(q, cu, kp, vp, bt, cl, scale, *a, **k):
                          scale, *a, **k)
 
 
+def _prefill_head_scales_by_q_head(q, cu, kp, vp, bt, cl, scale, kv_dtype="bf16",
+                                   k_scale=1.0, v_scale=1.0, k_scales=None, v_scales=None):
+    """Per-head FP8 scales looked up by q head (modulo the kv heads) instead
+    of by the q head's kv head."""
+    if k_scales is None:
+        return _real_prefill(q, cu, kp, vp, bt, cl, scale, kv_dtype, k_scale, v_scale)
+    hkv, Hq = kp.shape[1], q.shape[1]
+    out = np.zeros(q.shape, np.float64)
+    for a in range(Hq):
+        out[:, a] = _real_prefill(q[:, [a]], cu, kp[:, [a // (Hq // hkv)]],
+                                  vp[:, [a // (Hq // hkv)]], bt, cl, scale, kv_dtype,
+                                  float(k_scales[a % hkv]), float(v_scales[a % hkv]))[:, 0]
+    return out
+
+
+def _prefill_fp8_scales_swapped(q, cu, kp, vp, bt, cl, scale, kv_dtype="bf16", k_scale=1.0,
+                                v_scale=1.0, k_scales=None, v_scales=None):
+    return _real_prefill(q, cu, kp, vp, bt, cl, scale, kv_dtype, v_scale, k_scale,
+                         k_scales=v_scales, v_scales=k_scales)
+
+
 def _append_slot_plus_one(k_new, v_new, slots, kp, vp, *a, **k):
     return _real_append(k_new, v_new, (np.asarray(slots) + 1).astype(np.int64), kp, vp, *a, **k)
 
@@ -215,7 +236,10 @@ def _failing_calls(monkeypatch, attr, impl, calls):
 
 _PREFILL_PINS = [(n, ()) for n in ("test_prefill_matches_masked_dense_sdpa",
                                    "test_prefill_chunk_of_one_equals_decode",
-                                   "test_prefill_row_equals_truncated_decode")]
+                                   "test_prefill_row_equals_truncated_decode",
+                                   "test_prefill_fp8_row_equals_truncated_decode_with_head_scales")]
+_PREFILL_PINS += [("test_prefill_fp8_matches_masked_dense_dequantised", (ph,))
+                  for ph in (False, True)]
 _APPEND_PINS = [(n, ()) for n in ("test_kv_append_scatter_read_back",
                                   "test_kv_append_out_of_pool_counted_and_skipped",
                                   "test_kv_append_fp8_matches_torch_quantisation",
@@ -227,7 +251,8 @@ def test_prefill_and_append_oracles_pass_these_pins(monkeypatch):
     assert _failing_calls(monkeypatch, "kv_append", _real_append, _APPEND_PINS) == []
 
 
-@pytest.mark.parametrize("mutant", [_prefill_one_key_more, _prefill_own_key_masked])
+@pytest.mark.parametrize("mutant", [_prefill_one_key_more, _prefill_own_key_masked,
+                                    _prefill_head_scales_by_q_head, _prefill_fp8_scales_swapped])
 def test_a_planted_prefill_mistake_fails_a_pin(monkeypatch, mutant):
     assert _failing_calls(monkeypatch, "paged_prefill", mutant, _PREFILL_PINS)
 
