@@ -71,18 +71,19 @@ def _src_hash(name):
 
 
 def _ncu_traffic(kernel, workload_name):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+    """DRAM bytes per launch from profiles/traffic.json (ncu captures), if
+    the entry was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     src = {"decode_kernel": "decode.cu", "decode_mma_kernel": "decode_mma.cu",
            "prefill_kernel": "prefill.cu"}[kernel]
     want = _src_hash(src)
-    for line in open(path):
-        m = re.match(r"\s*-\s*traffic:\s*(\S+)\s+(\S+)\s+bytes_per_launch=(\d+)\s+src=(\w+)", line)
-        if m and m.group(1) == kernel and m.group(2) == workload_name and m.group(4) == want:
-            return int(m.group(3))
+    with open(path) as f:
+        entries = json.load(f).get("entries", [])
+    for e in entries:
+        if e["kernel"] == kernel and e["workload"] == workload_name and e["src"] == want:
+            return int(e["bytes_per_launch"])
     return None
 
 
@@ -375,32 +376,27 @@ def _packed(tensors, device):
     return buf, views
 
 
-def run_gpu(args):
+# Other workloads measured in the same run as the headline one, each with its
+# own step count (timed regions of tens of milliseconds, whatever --steps is).
+OTHER_WORKLOADS = ((3, 300), (4, 150), (5, 400), ("mixed_fp8", 400), (1, 400),
+                   ("long_prefill", 100))
+
+
+def _measure(w, a, dev, peaks, peak_kind, world):
+    """Time `a.steps` steps of workload w (after `a.warmup` untimed ones) and
+    return the report for it: value, rooflines, e2e, clocks."""
     import torch
 
     import paged_kv_attention_31_gb300 as pkv
-    from tests._gpu_state import device_pools, device_step_inputs
+    from device_inputs import device_pools, device_step_inputs
 
-    world, rank, local = _dist()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = _workload(args.workload, args.num_seqs)
-    peaks, peak_kind = _peaks()
-    l2_bytes = _l2_plan(w, args, dev)
-
-    # --- inputs resident in HBM ---------------------------------------------------
+    _, rank, local = _dist()
+    l2_bytes = _l2_plan(w, a, dev)
     d = device_step_inputs(w, dev)
     kp, vp = device_pools(w, dev)
-    cpu_line = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_line = cpu_baseline(w, args.cpu_sample_s, dev)
     B, Hq, D = w.num_seqs, w.num_q_heads, w.head_dim
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-    ws_bytes = pkv.paged_attention_workspace_size(B, Hq, w.max_context_len, kp, args.partition,
+    ws_bytes = pkv.paged_attention_workspace_size(B, Hq, w.max_context_len, kp, a.partition,
                                                   w.k_scale, w.v_scale)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     has_prefill = w.num_prefill > 0
@@ -412,34 +408,35 @@ def run_gpu(args):
     # rows are appended: by default the decode call runs on a high-priority
     # stream beside the prefill, so each fills the SMs the other's tail leaves
     # idle (the append then is its own call, ahead of both).
-    args.concurrent = has_prefill and not args.mixed_serial
-    if args.concurrent:
-        args.fused = False
+    a.concurrent = has_prefill and not a.mixed_serial
+    if a.concurrent:
+        a.fused = False
         hi_s = torch.cuda.Stream(dev, priority=-1)
         ev_app, ev_dec = torch.cuda.Event(), torch.cuda.Event()
 
     def step(q, k_new, v_new, slots, bt, cl, qp=None, cu=None, pbt=None, pcl=None, ev=None,
              o=None, op=None, decode_only=False):
         o = out if o is None else o
-        if args.concurrent and ev is None and not decode_only:
+        if a.concurrent and ev is None and not decode_only:
             m = torch.cuda.current_stream(dev)  # the capture stream under --graph
             pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
             ev_app.record(m)
             hi_s.wait_event(ev_app)
             pkv.paged_prefill(qp, cu, kp, vp, pbt, pcl, max_q, w.scale,
-                              out=out_p if op is None else op)
+                              out=out_p if op is None else op, k_scale=w.k_scale,
+                              v_scale=w.v_scale)
             pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
                                 workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
-                                partition_tokens=args.partition, stream=hi_s)
+                                partition_tokens=a.partition, stream=hi_s)
             ev_dec.record(hi_s)
             m.wait_event(ev_dec)
             return
-        if args.fused:  # the append runs inside the attention call's planning launch
+        if a.fused:  # the append runs inside the attention call's planning launch
             if ev is not None:
                 ev[0].record(stream)
             pkv.paged_attention_append(q, k_new, v_new, slots, kp, vp, bt, cl, w.max_context_len,
                                        w.scale, out=o, workspace=ws, k_scale=w.k_scale,
-                                       v_scale=w.v_scale, partition_tokens=args.partition)
+                                       v_scale=w.v_scale, partition_tokens=a.partition)
         else:
             if not decode_only:  # a decode-only pass times the attention call alone
                 pkv.kv_append(k_new, v_new, slots, kp, vp, w.k_scale, w.v_scale)
@@ -447,14 +444,15 @@ def run_gpu(args):
                 ev[0].record(stream)
             pkv.paged_attention(q, kp, vp, bt, cl, w.max_context_len, w.scale, out=o,
                                 workspace=ws, k_scale=w.k_scale, v_scale=w.v_scale,
-                                partition_tokens=args.partition)
+                                partition_tokens=a.partition)
         if ev is not None:
             ev[1].record(stream)
         if has_prefill and not decode_only:
             if ev is not None:
                 ev[2].record(stream)
             pkv.paged_prefill(qp, cu, kp, vp, pbt, pcl, max_q, w.scale,
-                              out=out_p if op is None else op)
+                              out=out_p if op is None else op, k_scale=w.k_scale,
+                              v_scale=w.v_scale)
             if ev is not None:
                 ev[3].record(stream)
 
@@ -462,14 +460,14 @@ def run_gpu(args):
     if has_prefill:
         args_dev += (d["q_prefill"], d["cu_seqlens_q"], d["prefill_block_tables"],
                      d["prefill_context_lens"])
-    for _ in range(args.warmup):
+    for _ in range(a.warmup):
         step(*args_dev)
     torch.cuda.synchronize(dev)
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
     graph = None
-    if args.graph:
+    if a.graph:
         # the whole step captured once and replayed (per-kernel timing for the
         # roofline then comes from a short eager loop below)
         side = torch.cuda.Stream(dev)
@@ -481,7 +479,7 @@ def run_gpu(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step(*args_dev)
-        for _ in range(args.warmup):
+        for _ in range(a.warmup):
             graph.replay()
         torch.cuda.synchronize(dev)
 
@@ -493,12 +491,12 @@ def run_gpu(args):
     # the L2 is flushed (a write of twice its size) before every step,
     # outside the timed spans, and each step is timed on its own.
     flush_buf = None
-    if args.flush:
+    if a.flush:
         flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
     evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
-           for _ in range(args.steps)]
+           for _ in range(a.steps)]
     spans = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
-             for _ in range(args.steps)] if args.flush else None
+             for _ in range(a.steps)] if a.flush else None
     clocks = ClockSampler(local)
     clocks.start()
     if world > 1:
@@ -507,7 +505,7 @@ def run_gpu(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(a.steps):
         if spans is not None:
             flush_buf.fill_(i & 255)
             spans[i][0].record(stream)
@@ -521,7 +519,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     # per-call timing for the rooflines: the same steps again (eager), CUDA
     # events on the launching stream around each call
-    for i in range(args.steps):
+    for i in range(a.steps):
         if flush_buf is not None:
             flush_buf.fill_(i & 255)
         step(*args_dev, ev=evs[i])
@@ -532,16 +530,16 @@ def run_gpu(args):
         c0 = torch.cuda.Event(enable_timing=True)
         c1 = torch.cuda.Event(enable_timing=True)
         c0.record(stream)
-        for i in range(args.steps):
+        for i in range(a.steps):
             step(*args_dev, decode_only=True)
         c1.record(stream)
         torch.cuda.synchronize(dev)
-        dec_chain_ms = c0.elapsed_time(c1) / args.steps
+        dec_chain_ms = c0.elapsed_time(c1) / a.steps
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
     elapsed_ms = (t_start.elapsed_time(t_stop) if spans is None
-                  else float(sum(a.elapsed_time(b) for a, b in spans)))
+                  else float(sum(x.elapsed_time(y) for x, y in spans)))
     attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     prefill_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs])) if has_prefill else None
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
@@ -590,7 +588,7 @@ def run_gpu(args):
             ohost[b][0].copy_(osets[b][0], non_blocking=True)
         ev_out[b].record(d2h_s)
 
-    for i in range(min(args.warmup, 3)):
+    for i in range(min(a.warmup, 3)):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     if flush_buf is None:
@@ -598,17 +596,17 @@ def run_gpu(args):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         h2d_s.wait_event(e0)
-        for i in range(args.steps):
+        for i in range(a.steps):
             e2e_step(i)
         for b in range(nbuf):
             stream.wait_event(ev_out[b])
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        last = ohost[(args.steps - 1) % nbuf][1][0]
-        e2e_ms = e0.elapsed_time(e1) / args.steps
+        last = ohost[(a.steps - 1) % nbuf][1][0]
+        e2e_ms = e0.elapsed_time(e1) / a.steps
     else:  # L2 flushed before each step (untimed); copies and kernels in one stream
         e2e_spans = []
-        for i in range(args.steps):
+        for i in range(a.steps):
             flush_buf.fill_(i & 255)
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
@@ -620,7 +618,7 @@ def run_gpu(args):
             e2e_spans.append((a0, a1))
         torch.cuda.synchronize(dev)
         last = ohost[0][1][0]
-        e2e_ms = float(sum(x.elapsed_time(y) for x, y in e2e_spans)) / args.steps
+        e2e_ms = float(sum(x.elapsed_time(y) for x, y in e2e_spans)) / a.steps
     if not torch.equal(last, out.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident run")
     if pkv.get_device_error() != 0:
@@ -628,12 +626,12 @@ def run_gpu(args):
 
     # --- report ----------------------------------------------------------------------
     step_bytes = w.decode_step_bytes()
-    ms = elapsed_ms / args.steps
+    ms = elapsed_ms / a.steps
     value = replica_throughput(step_bytes, world, ms)
     attn_bytes = (w.decode_kv_bytes() + 2 * B * Hq * D * 2 +
                   int(np.sum((w.context_lens.astype(np.int64) + w.block_size - 1)
                              // w.block_size)) * 4 + B * 4)
-    if args.fused:  # the timed call also scatters the appended rows (all of them:
+    if a.fused:  # the timed call also scatters the appended rows (all of them:
         # with prefill chunks in the step, their rows too)
         n_app = w.num_append_tokens
         attn_bytes += n_app * w.num_kv_heads * D * (2 * 2 + 2 * w.elem_bytes) + n_app * 8
@@ -646,24 +644,25 @@ def run_gpu(args):
     # 4 or 8 q heads per kv head at head_dim 128 run on the tensor-core decode
     kname = ("decode_mma_kernel" if D == 128 and w.group in (4, 8) and w.block_size >= 16
              else "decode_kernel")
-    launches_per_step = (2 if args.fused else 3) + (1 if has_prefill else 0)
+    launches_per_step = (2 if a.fused else 3) + (1 if has_prefill else 0)
     # append, plan, decode (+ prefill); fused: plan-and-append, decode
-    part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, args.partition,
+    part, max_splits = pkv.paged_attention_plan(B, Hq, w.max_context_len, kp, a.partition,
                                                 w.k_scale, w.v_scale)
     splits = max_splits > 1
     launches_per_step += 1 if splits else 0
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 kv, bf16 q/out",
-        "data": "synthetic", "config": _config(w, args),
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 kv, bf16 q/out",
+        "data": "synthetic", "config": _config(w, a),
         # every sequence of the iteration advances one step (prefill chunks too)
         "seq_steps_per_s": world * (B + w.num_prefill) / (ms * 1e-3),
         "frac_of_hbm_peak": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": (f"{kname} (pkv_paged_attention_append: plan and append + "
-                                "decode + merge)" if args.fused else
+                                "decode + merge)" if a.fused else
                                 f"{kname} (pkv_paged_attention: plan + decode + merge)"),
                      "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": attn_ms,
                      "timing": "CUDA events around each call (second pass over the steps)",
@@ -677,12 +676,12 @@ def run_gpu(args):
                                     "the timed steps (the step is this call)")}},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * a.steps,
         "clocks": clock_info,
     }
     if w.num_sharers > 1:  # shared prefix pages counted once above; per sequence here
-        line["logical_kv_gbs"] = (w.decode_kv_bytes(unique=False) + (attn_bytes - w.decode_kv_bytes())) \
-            / (attn_ms * 1e-3) / 1e9
+        line["logical_kv_gbs"] = (w.decode_kv_bytes(unique=False) +
+                                  (attn_bytes - w.decode_kv_bytes())) / (attn_ms * 1e-3) / 1e9
     if has_prefill:
         tokens = B + int(np.sum(w.prefill_chunk_lens))
         line["sequences_per_iteration"] = B + w.num_prefill
@@ -696,12 +695,144 @@ def run_gpu(args):
         line["decode_roofline"] = line["roofline"]
         line["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": tpeak,
                             "unit": "TFLOP/s", "frac": tflops / tpeak, "peak_kind": peak_kind,
-                            "kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
+                            "kernel": ("prefill_kernel (pkv_paged_prefill, tcgen05, "
+                                       + ("f16 operands from the FP8 pool)"
+                                          if w.kv_dtype != "bf16" else "bf16 operands)")),
                             "algorithmic_flops_per_launch": flops, "ms_per_launch": prefill_ms,
                             "timing": "CUDA events around each call (second pass over the steps)",
                             "traffic": _ncu_traffic("prefill_kernel", w.name)}
+    del kp, vp, d, ws, out
+    torch.cuda.empty_cache()
+    return line
+
+
+def _measure_prefill_only(w, a, dev, peaks, peak_kind, world):
+    """Chunked prefill alone (its rows appended once, untimed): the prefill
+    call timed back to back over a.steps calls, then with events around each
+    call; tensor roofline against the bf16 peak."""
+    import torch
+
+    import paged_kv_attention_31_gb300 as pkv
+    from device_inputs import device_pools, device_step_inputs
+
+    _, _, local = _dist()
+    d = device_step_inputs(w, dev)
+    kp, vp = device_pools(w, dev)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale)
+    max_q = int(w.prefill_chunk_lens.max())
+    out_p = torch.empty_like(d["q_prefill"])
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp, d["prefill_block_tables"],
+                          d["prefill_context_lens"], max_q, w.scale, out=out_p,
+                          k_scale=w.k_scale, v_scale=w.v_scale)
+
+    for _ in range(a.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(a.steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    for e in evs:
+        e[0].record(stream)
+        call()
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during the prefill timing")
+    chain_ms = max_over_ranks(t0.elapsed_time(t1) / a.steps, dev)
+    call_ms = float(np.mean([x.elapsed_time(y) for x, y in evs]))
+    flops = w.prefill_flops()
+    tpeak = float(peaks["bf16_tflops"])
+    value = world * flops / (chain_ms * 1e-3) / 1e12
+    line = {
+        "value": value, "unit": "TFLOP/s", "ms_per_step": chain_ms, "steps": a.steps,
+        "warmup": a.warmup, "higher_is_better": True,
+        "config": {"workload": w.name, "prefill_chunks": [int(x) for x in w.prefill_chunk_lens],
+                   "prior_context_lens": [int(x) for x in
+                                          w.prefill_context_lens - w.prefill_chunk_lens],
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block_size": w.block_size,
+                   "kv_dtype": w.kv_dtype, "step_calls": "pkv_paged_prefill"},
+        "tokens_per_s": world * w.num_prefill_tokens / (chain_ms * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": flops / (call_ms * 1e-3) / 1e12,
+                     "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": flops / (call_ms * 1e-3) / 1e12 / tpeak, "peak_kind": peak_kind,
+                     "kernel": "prefill_kernel (pkv_paged_prefill, tcgen05)",
+                     "algorithmic_flops_per_launch": flops, "ms_per_launch": call_ms,
+                     "timing": "CUDA events around each call",
+                     "traffic": _ncu_traffic("prefill_kernel", w.name),
+                     "back_to_back": {"ms_per_launch": chain_ms,
+                                      "achieved": flops / (chain_ms * 1e-3) / 1e12,
+                                      "frac": flops / (chain_ms * 1e-3) / 1e12 / tpeak,
+                                      "timing": "the calls back to back, one event pair around "
+                                                "the loop"}},
+        "gpu_launches": a.steps,
+        "clocks": clock_info,
+    }
+    del kp, vp, d, out_p
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_gpu(args):
+    import copy
+
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = _peaks()
+    w = _workload(args.workload, args.num_seqs)
+    cpu_line = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.num_seqs > 0:
+        cpu_line = cpu_baseline(w, args.cpu_sample_s, dev)
+    if w.num_seqs == 0:  # the long prefill: no decode sequences, no CPU decode sample
+        line = _measure_prefill_only(w, args, dev, peaks, peak_kind, world)
+        line.update({"metric": "paged chunked-prefill attention TFLOP/s (causal-exact flops)",
+                     "n_gpus": world, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                     "data": "synthetic"})
+        cpu_line = None
+    else:
+        line = _measure(w, args, dev, peaks, peak_kind, world)
     if cpu_line is not None:
         line["cpu_baseline"], line["cpu_baseline_all_cores"] = cpu_line
+    if not args.no_other_workloads and args.num_seqs is None:
+        # every other configuration in the same process, each with its own
+        # step count: the headline above stays this run's `value`
+        others = {}
+        for wid, steps in OTHER_WORKLOADS:
+            if wid == args.workload:
+                continue
+            a = copy.copy(args)
+            a.steps, a.warmup, a.graph, a.fused, a.mixed_serial = steps, 10, False, True, False
+            a.partition = 0
+            wo = _workload(wid)
+            m = (_measure_prefill_only if wo.num_seqs == 0 else _measure)(
+                wo, a, dev, peaks, peak_kind, world)
+            m.pop("metric", None)
+            others[wo.name] = m
+        line["workloads"] = others
+        line["gpu_launches"] += sum(m["gpu_launches"] for m in others.values())
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -715,7 +846,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    type=lambda x: int(x) if x.isdigit() else x,
+                    choices=[1, 2, 3, 4, 5, "mixed_fp8", "long_prefill"])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition tokens (0 = library's automatic choice)")
     ap.add_argument("--separate-append", dest="fused", action="store_false",
@@ -732,10 +865,15 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
     ap.add_argument("--ref-sample-s", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="measure only --workload (by default every other configuration, and "
+                         "the long-context prefill, follow in the same run under 'workloads')")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.workload == "long_prefill":
+            ap.error("the reference arm times the decode step: pick a workload 1..5")
         return run_reference(args)
     return run_gpu(args)
 

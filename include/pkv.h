@@ -221,14 +221,20 @@ PKV_API size_t pkv_paged_attention_noalloc_max_scratch(void);
  *   q               device, bf16 [num_q_tokens][num_q_heads][head_dim], 16-byte aligned
  *   cu_seqlens_q    device, int32 [num_seqs + 1], non-decreasing, [0] = 0,
  *                   [num_seqs] = num_q_tokens, each C_s <= min(max_q_len, L_s)
- *   k_pool, v_pool  device pools (bf16 only), 16-byte aligned
+ *   k_pool, v_pool  device pools, bf16 or FP8 E4M3 (scales as in the pool
+ *                   descriptor: k_scale multiplies the scores, v_scale the
+ *                   output), 16-byte aligned
  *   block_tables    device, int32 [num_seqs][max_blocks_per_seq]
  *   context_lens    device, int32 [num_seqs]
  *   max_q_len       host upper bound of C_s
  *   scale           softmax scale, finite and > 0
  *   out             device, bf16 [num_q_tokens][num_q_heads][head_dim]
- * head_dim 64 or 128 and a bf16 pool (FP8 pools: PKV_ERR_UNSUPPORTED); the
- * group size num_q_heads/num_kv_heads must divide 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.
+ * head_dim 64 or 128; the group size num_q_heads/num_kv_heads must divide
+ * 128.  Uses tcgen05 tensor cores and TMA; needs no workspace.  An FP8 pool
+ * is dequantised inside the kernel (§7.2, its third item): the codes are
+ * converted exactly to f16 in shared memory, q is converted to f16 after an
+ * exact power-of-two scaling per query row (undone on the scores), and both
+ * products run on f16 operands with fp32 accumulation.
  * Device data: a sequence whose rows fall outside 0 .. num_q_tokens-1, whose
  * chunk is longer than max_q_len or than L_s, or whose L_s exceeds
  * max_blocks_per_seq pages is skipped (its rows are not written) and
@@ -244,10 +250,14 @@ PKV_API pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_seqlens_q,
                              void *stream);
 
 /*
- * pkv_get_device_error -- synchronise `stream`, then read and clear the
- * current device's sticky error word.  *code receives PKV_OK,
+ * pkv_get_device_error -- read and clear the current device's sticky error
+ * word after the work already enqueued on `stream`: one small kernel on
+ * `stream` swaps the word for zero atomically, the value is copied back on
+ * the same stream and the stream is synchronised.  *code receives PKV_OK,
  * PKV_ERR_DEVICE_BOUNDS or PKV_ERR_DEVICE_TIMEOUT (the first error recorded
- * since the last call).  Returns PKV_ERR_CUDA if the synchronisation fails.
+ * since the last read).  An error that a kernel on another stream records
+ * meanwhile is returned by this read or kept for the next one, never lost.
+ * Returns PKV_ERR_CUDA if the launch, the copy or the synchronisation fails.
  */
 PKV_API pkv_status pkv_get_device_error(int32_t *code, void *stream);
 

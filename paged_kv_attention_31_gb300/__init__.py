@@ -2,7 +2,9 @@
 
 Argument marshalling only: every step of the attention path runs in the CUDA
 kernels behind the C ABI declared in include/pkv.h.  Tensors are torch CUDA
-tensors; each call is enqueued on torch's current CUDA stream.  There is no
+tensors; each call is enqueued on torch's current CUDA stream, or on the
+`stream` argument when one is given (its default outputs and workspace are
+then allocated on that stream).  There is no
 CPU fallback: if the compiled library is missing, importing a function raises.
 
 Functions mirror the C entry points:
@@ -20,6 +22,7 @@ Functions mirror the C entry points:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -148,6 +151,14 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on(stream):
+    """Context in which a call allocates its default tensors: the stream the
+    call is enqueued on, so the caching allocator ties them to that stream
+    and cannot hand their memory to another stream's allocation while the
+    call's kernels still use it."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     if t is None:
         return ctypes.c_void_p(0)
@@ -255,13 +266,14 @@ def paged_attention(q, k_pool, v_pool, block_tables, context_lens, max_context_l
         raise TypeError("block_tables / context_lens must be int32")
     desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     B, Hq, D = q.shape
-    if out is None:
-        out = torch.empty_like(q)
-    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
-    if workspace is None:
-        nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool,
-                                                partition_tokens, k_scale, v_scale)
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
+        if workspace is None:
+            nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool,
+                                                    partition_tokens, k_scale, v_scale)
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     _check(lib().pkv_paged_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), ctypes.byref(desc),
                                      _ptr(block_tables), int(block_tables.shape[1]),
                                      _ptr(context_lens), int(B), int(Hq), int(max_context_len),
@@ -293,13 +305,14 @@ def paged_attention_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_
     if tuple(k_new.shape) != (T, desc.num_kv_heads, desc.head_dim) or k_new.shape != v_new.shape:
         raise ValueError("k_new / v_new must be [T, num_kv_heads, head_dim]")
     B, Hq, D = q.shape
-    if out is None:
-        out = torch.empty_like(q)
-    _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
-    if workspace is None:
-        nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool, partition_tokens,
-                                                k_scale, v_scale)
-        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
+        if workspace is None:
+            nbytes = paged_attention_workspace_size(B, Hq, max_context_len, k_pool,
+                                                    partition_tokens, k_scale, v_scale)
+            workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     _check(lib().pkv_paged_attention_append(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(k_pool), _ptr(v_pool),
         ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
@@ -322,7 +335,8 @@ def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_c
     desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        with _on(stream):
+            out = torch.empty_like(q)
     _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, B)
     _check(lib().pkv_paged_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
                                              ctypes.byref(desc), _ptr(block_tables),
@@ -334,18 +348,21 @@ def paged_attention_noalloc(q, k_pool, v_pool, block_tables, context_lens, max_c
 
 
 def paged_prefill(q, cu_seqlens_q, k_pool, v_pool, block_tables, context_lens, max_q_len,
-                  scale, out=None, stream=None) -> torch.Tensor:
-    """Causal chunked-prefill attention: q [T, Hq, D] bf16 -> out [T, Hq, D] bf16."""
+                  scale, out=None, stream=None, k_scale=1.0, v_scale=1.0, k_scales=None,
+                  v_scales=None) -> torch.Tensor:
+    """Causal chunked-prefill attention: q [T, Hq, D] bf16 -> out [T, Hq, D]
+    bf16, over a bf16 or FP8 (E4M3, per-tensor or per-kv-head scales) pool."""
     if q.dtype != torch.bfloat16 or q.dim() != 3:
         raise TypeError("q must be bfloat16 [num_q_tokens, num_q_heads, head_dim]")
     for t in (cu_seqlens_q, block_tables, context_lens):
         if t.dtype != torch.int32:
             raise TypeError("cu_seqlens_q / block_tables / context_lens must be int32")
-    desc = pool_desc(k_pool)
+    desc = pool_desc(k_pool, k_scale, v_scale, k_scales, v_scales)
     T, Hq, D = q.shape
     n = int(context_lens.shape[0])
     if out is None:
-        out = torch.empty_like(q)
+        with _on(stream):
+            out = torch.empty_like(q)
     _check_shapes(q, k_pool, v_pool, block_tables, context_lens, out, desc, n)
     if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] != n + 1:
         raise ValueError("cu_seqlens_q must be [num_seqs + 1]")
@@ -469,10 +486,13 @@ class KVCacheManager:
 def self_test_bounded_wait(limit_cycles: int = 1_000_000, stream=None) -> list:
     """Run the failure-path check (pkv_self_test_bounded_wait) and return its
     five results; the device error word then holds PKV_ERR_DEVICE_TIMEOUT."""
-    out = torch.full((5,), -1, dtype=torch.int32, device="cuda")
-    _check(lib().pkv_self_test_bounded_wait(int(limit_cycles), _ptr(out), _stream(stream)),
-           "pkv_self_test_bounded_wait")
-    return [int(x) for x in out.cpu()]
+    # the buffer, the kernel and the read-back all on the call's stream: the
+    # copy to the host waits for the kernel
+    with _on(stream):
+        out = torch.full((5,), -1, dtype=torch.int32, device="cuda")
+        _check(lib().pkv_self_test_bounded_wait(int(limit_cycles), _ptr(out), _stream(stream)),
+               "pkv_self_test_bounded_wait")
+        return [int(x) for x in out.cpu()]
 
 
 def get_device_error(stream=None) -> int:

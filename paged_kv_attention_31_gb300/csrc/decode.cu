@@ -387,7 +387,15 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       const uint32_t parity = ((jt + j) / ST) & 1;
       const int ts = t0 + (warp + j * NW) * TT;
       const int ntok = pages[ts / P - pg0] < 0 ? 0 : min(TT, t1 - ts);
-      mbar_wait_bounded(&bars[stage], parity, p.err, abort_flag);
+      if (!warp_wait_bounded(&bars[stage], parity, p.err, abort_flag)) {
+        // a wait gave up: compute nothing more; let this warp's copies in
+        // flight (tiles j .. j + ST - 1) land before the CTA leaves
+        if (lane == 0)
+          for (int jj = j; jj < min(j + ST, my_n); ++jj)
+            mbar_drain_wait(&bars[(jt + jj) % ST], ((jt + jj) / ST) & 1, p.err);
+        __syncwarp();
+        break;
+      }
       const uint8_t* kb = kbuf + stage * TB;
       const uint8_t* vb = vbuf + stage * TB;
 
@@ -512,7 +520,12 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
     if (threadIdx.x == 0) misc[1] = next;
     __syncthreads();
     const int next_unit = misc[1];
-    for (int idx = threadIdx.x; idx < G * D; idx += C::NTHR) {
+    // The abort flag changes only inside the tile loops: between the
+    // barrier above and the next unit's first barrier every thread reads the
+    // same value.  After an abort the unit's results are not written and the
+    // CTA takes no further work.
+    const bool aborted = *abort_flag != 0;
+    for (int idx = threadIdx.x; idx < G * D && !aborted; idx += C::NTHR) {
       const int g = idx / D, d = idx - g * D;
       float M = -INFINITY;
 #pragma unroll
@@ -538,6 +551,7 @@ __global__ void __launch_bounds__(kNW * 32) decode_kernel(const DecodeParams p) 
       }
     }
     __syncthreads();  // shared state is reused by the next unit
+    if (aborted) break;
     unit = next_unit;
   }
   pdl_launch_dependents();  // out of work: the merge may launch

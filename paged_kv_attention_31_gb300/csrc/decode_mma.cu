@@ -10,7 +10,8 @@
 // FP8 not at all); here each warp does the per-tile contractions with
 // mma.sync m16n8k16 with fp32 accumulation: bf16 x bf16 for bf16 KV, and
 // f16 x f16 for FP8 KV with the E4M3 codes converted to f16 (exactly) in
-// registers.
+// registers and each head's q scaled by a power of two into f16's range
+// (exact; the scores are scaled back).
 //
 // Per 16-token tile (one warp, lane = 4 r + c):
 //   QK  S^T[16 tokens x 8 heads] = K[16 x 128] q^T: M = tokens, N = heads
@@ -21,7 +22,9 @@
 //       its share of rows r and r + 8 with 16-byte loads.
 //   softmax per head over the 16 tokens: the scores of head 2c + {0,1} sit in
 //       the 8 lanes with the same c (xor-4/8/16 butterflies); running max and
-//       sum in the log2 domain; P in f16 (exact running max, so P <= 1).
+//       sum in the log2 domain; P rounded to the MMA's type (bf16 for bf16
+//       KV, f16 for FP8 KV; the running max is exact, so P <= 1), the row
+//       sum taken over the unrounded fp32 values.
 //   PV  O^T[128 x 8] += V^T[128 x 16 tokens] P^T: M = head_dim (8 tiles of
 //       16), N = heads, K = tokens.  The M index is permuted so that lane r
 //       owns 16 head_dim values (FP8: 16r .. 16r + 15; bf16: two 8-value
@@ -208,24 +211,63 @@ __global__ void __launch_bounds__(kNW * 32)
     // B fragments of q for the 8 reduction steps (head g = r, zero past G):
     // qb[2s] holds the first, qb[2s+1] the second pair of step s
     uint32_t qb[16];
+    // FP8: the unscale factors 2^-k of heads 2c and 2c + 1 (see below)
+    float q_unscale[2] = {1.f, 1.f};
     {
       const int g = r;
-      if (g < G) {
-        const __nv_bfloat16* qrow =
-            static_cast<const __nv_bfloat16*>(p.q) + (size_t(s) * p.num_q_heads + size_t(h) * G + g) * kD;
-        if constexpr (FP8) {  // head_dim 32c .. 32c + 31, converted to f16
-          const uint4* src = reinterpret_cast<const uint4*>(qrow + 32 * c);
+      if constexpr (FP8) {
+        // head_dim 32c .. 32c + 31 of head g, as f16.  f16 holds every bf16
+        // value of magnitude 2^-14 .. 65280 exactly but not the rest of
+        // bf16's range, so each head's q is first multiplied by an exact
+        // power of two 2^k that puts its largest |q| in [2^15, 2^16); the
+        // scores of that head are multiplied by 2^-k afterwards.  Elements
+        // more than 2^29 below the head's largest stay within f16's normal
+        // range; smaller ones round to f16 subnormals, far below the fp32
+        // accumulation error of the dot product.
+        uint4 u[4] = {};
+        float amax = 0.f;
+        if (g < G) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(p.q) +
+              (size_t(s) * p.num_q_heads + size_t(h) * G + g) * kD + 32 * c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint4 u = __ldg(src + i);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            u[i] = __ldg(src + i);
+            const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float2 f = bf16x2_to_float2(w[j]);
-              qb[4 * i + j] = pack2<true>(f.x, f.y);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
             }
           }
-        } else {  // head_dim 16c .. 16c + 15 and 64 + 16c .. 64 + 16c + 15, as is
+        }
+        // the 4 lanes of head g (lane = 4g + c) hold its 128 elements
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // k = 15 - floor(log2 amax), clamped to [-126, 126] so that 2^k and
+        // 2^-k are normal floats (a head whose largest |q| is an fp32
+        // subnormal ends up below 2^15, still inside f16's range); an
+        // all-zero head keeps k = 0
+        const int e = int((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // -127 if subnormal
+        const int k = amax > 0.f ? max(-126, min(126, 15 - e)) : 0;
+        const float up = __uint_as_float(uint32_t(127 + k) << 23);
+        const float down = __uint_as_float(uint32_t(127 - k) << 23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = bf16x2_to_float2(w[j]);
+            qb[4 * i + j] = pack2<true>(f.x * up, f.y * up);  // exact products
+          }
+        }
+        // heads 2c and 2c + 1 own this lane's score columns
+        q_unscale[0] = __shfl_sync(0xffffffffu, down, 4 * (2 * c));
+        q_unscale[1] = __shfl_sync(0xffffffffu, down, 4 * (2 * c + 1));
+      } else if (g < G) {
+        const __nv_bfloat16* qrow =
+            static_cast<const __nv_bfloat16*>(p.q) + (size_t(s) * p.num_q_heads + size_t(h) * G + g) * kD;
+        {  // head_dim 16c .. 16c + 15 and 64 + 16c .. 64 + 16c + 15, as is
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * hf + 16 * c);
@@ -277,7 +319,15 @@ __global__ void __launch_bounds__(kNW * 32)
       const uint32_t parity = ((jt + j) / kST) & 1;
       const int ts = t0 + (warp + j * kNW) * kTT;
       const int ntok = pages[ts / P - pg0] < 0 ? 0 : min(kTT, t1 - ts);
-      mbar_wait_bounded(&bars[stage], parity, p.err, abort_flag);
+      if (!warp_wait_bounded(&bars[stage], parity, p.err, abort_flag)) {
+        // a wait gave up: compute nothing more; let this warp's copies in
+        // flight (tiles j .. j + kST - 1) land before the CTA leaves
+        if (lane == 0)
+          for (int jj = j; jj < min(j + kST, my_n); ++jj)
+            mbar_drain_wait(&bars[(jt + jj) % kST], ((jt + jj) / kST) & 1, p.err);
+        __syncwarp();
+        break;
+      }
       const uint8_t* kt = kbuf + stage * TB;
       const uint8_t* vt = vbuf + stage * TB;
 
@@ -317,6 +367,12 @@ __global__ void __launch_bounds__(kNW * 32)
       // sacc: [0] token r head 2c, [1] token r head 2c+1, [2] token r+8 head 2c,
       // [3] token r+8 head 2c+1
       const bool v0 = r < ntok, v1 = r + 8 < ntok;
+      if constexpr (FP8) {  // back from each head's 2^k-scaled q
+        sacc[0] *= q_unscale[0];
+        sacc[1] *= q_unscale[1];
+        sacc[2] *= q_unscale[0];
+        sacc[3] *= q_unscale[1];
+      }
       float sv[4] = {v0 ? sacc[0] * qm : -INFINITY, v0 ? sacc[1] * qm : -INFINITY,
                      v1 ? sacc[2] * qm : -INFINITY, v1 ? sacc[3] * qm : -INFINITY};
 
@@ -443,7 +499,12 @@ __global__ void __launch_bounds__(kNW * 32)
     if (threadIdx.x == 0) misc[1] = next;
     __syncthreads();
     const int next_unit = misc[1];
-    for (int idx = threadIdx.x; idx < G * kD; idx += kNW * 32) {
+    // The abort flag changes only inside the tile loops: between the
+    // barrier above and the next unit's first barrier every thread reads the
+    // same value.  After an abort the unit's results are not written and the
+    // CTA takes no further work.
+    const bool aborted = *abort_flag != 0;
+    for (int idx = threadIdx.x; idx < G * kD && !aborted; idx += kNW * 32) {
       const int g = idx / kD, d = idx - g * kD;
       float M = -INFINITY;
 #pragma unroll
@@ -470,6 +531,7 @@ __global__ void __launch_bounds__(kNW * 32)
     }
     fence_proxy_async_smem();  // the combine buffer is refilled by TMA next
     __syncthreads();           // shared state is reused by the next unit
+    if (aborted) break;
     unit = next_unit;
   }
   pdl_launch_dependents();  // out of work: the merge may launch

@@ -58,14 +58,19 @@ pkv_status pkv_paged_attention_noalloc(const void* q, const void* k_pool, const 
                                        int32_t num_seqs, int32_t num_q_heads,
                                        int32_t max_context_len, float scale,
                                        int32_t partition_tokens, void* out, void* stream) {
-  if (num_seqs == 0) return PKV_OK;
+  // the argument checks of pkv_paged_attention, so that both report the
+  // same status for the same arguments
+  pkv_status st = pkv::decode_args_status(q, k_pool, v_pool, pool, block_tables,
+                                          max_blocks_per_seq, context_lens, num_seqs,
+                                          num_q_heads, max_context_len, scale, partition_tokens,
+                                          out);
+  if (st != PKV_OK || num_seqs == 0) return st;
   const size_t need = pkv_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len,
                                                          partition_tokens, pool);
   if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;  // beyond the fixed maximum
   void* scratch = nullptr;
-  const pkv_status st = scratch_address(&scratch);
-  if (st != PKV_OK) return st;
+  if ((st = scratch_address(&scratch)) != PKV_OK) return st;
   // The decode path needs no zeroed scratch: its planner kernel rewrites the
   // work counters and item list before the decode kernel reads them, and every
   // partial result is written before the merge reads it.

@@ -9,6 +9,8 @@
 
 // Sticky per-device error word written by the kernels (first error wins).
 __device__ int32_t g_pkv_device_error = 0;
+// Where pkv_get_device_error's exchange kernel leaves the word it took.
+__device__ int32_t g_pkv_device_error_taken = 0;
 
 namespace {
 
@@ -17,6 +19,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int num_sms = 0;
   int32_t* err = nullptr;
+  int32_t* taken = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::atomic<bool> g_dev_ready[kMaxDevices];
@@ -32,8 +35,12 @@ pkv_status device_info(DeviceInfo** out) {
     if (r != cudaSuccess) return r;
     r = cudaGetSymbolAddress(&addr, g_pkv_device_error);
     if (r != cudaSuccess) return r;
+    void* taken = nullptr;
+    r = cudaGetSymbolAddress(&taken, g_pkv_device_error_taken);
+    if (r != cudaSuccess) return r;
     d.num_sms = sms;
     d.err = static_cast<int32_t*>(addr);
+    d.taken = static_cast<int32_t*>(taken);
     return cudaSuccess;
   });
   if (e != cudaSuccess) return PKV_ERR_CUDA;
@@ -127,6 +134,11 @@ __global__ void self_test_wait_kernel(int32_t* err, long long limit, int32_t* ou
   out[3] = (t1 - t0) >= limit ? 1 : 0;
   out[4] = (t2 - t1) < limit / 4 ? 1 : 0;
 }
+
+// Read and clear the error word in one atomic step, so an error a kernel on
+// another stream records meanwhile is either returned now or kept for the
+// next read, never lost.
+__global__ void take_error_kernel(int32_t* err, int32_t* taken) { *taken = atomicExch(err, 0); }
 
 }  // namespace
 
@@ -256,15 +268,18 @@ pkv_status pkv_paged_attention_plan(int32_t num_seqs, int32_t num_q_heads,
   return PKV_OK;
 }
 
-// Decode attention; with `app`, the step's appends run in the planning launch.
-static pkv_status paged_attention_impl(const void* q, const void* k_pool, const void* v_pool,
-                                       const pkv_pool_desc* pool, const int32_t* block_tables,
-                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                       int32_t num_seqs, int32_t num_q_heads,
-                                       int32_t max_context_len, float scale,
-                                       int32_t partition_tokens, void* workspace,
-                                       size_t workspace_bytes, void* out, void* stream,
-                                       const pkv::AppendParams* app) {
+}  // extern "C"
+
+namespace pkv {
+
+// Host validation of a decode call's arguments other than its workspace, in
+// the order the status codes are reported; PKV_OK for num_seqs == 0 once the
+// sizes are valid (the pointers are then not looked at).
+pkv_status decode_args_status(const void* q, const void* k_pool, const void* v_pool,
+                              const pkv_pool_desc* pool, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                              float scale, int32_t partition_tokens, const void* out) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || max_blocks_per_seq <= 0)
@@ -275,12 +290,34 @@ static pkv_status paged_attention_impl(const void* q, const void* k_pool, const 
   if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if ((st = validate_partition(partition_tokens, pool->block_size)) != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
-  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || !workspace)
+  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3))
     return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+// Decode attention; with `app`, the step's appends run in the planning launch.
+static pkv_status paged_attention_impl(const void* q, const void* k_pool, const void* v_pool,
+                                       const pkv_pool_desc* pool, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t max_context_len, float scale,
+                                       int32_t partition_tokens, void* workspace,
+                                       size_t workspace_bytes, void* out, void* stream,
+                                       const pkv::AppendParams* app) {
+  pkv_status st = pkv::decode_args_status(q, k_pool, v_pool, pool, block_tables,
+                                          max_blocks_per_seq, context_lens, num_seqs,
+                                          num_q_heads, max_context_len, scale, partition_tokens,
+                                          out);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  if (!workspace) return PKV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PKV_OK) return st;
@@ -379,7 +416,6 @@ pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const v
                              void* stream) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
-  if (pool->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || num_q_tokens < 0 ||
       max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -413,7 +449,13 @@ pkv_status pkv_paged_prefill(const void* q, const int32_t* cu_seqlens_q, const v
   p.num_blocks = pool->num_blocks;
   p.num_q_tokens = num_q_tokens;
   p.tiles_per_seq = (int)((int64_t(max_q_len) * G + 127) / 128);
-  p.q_mult = scale * 1.4426950408889634f;
+  const bool fp8 = pool->kv_dtype == PKV_KV_FP8_E4M3;
+  p.fp8 = fp8;
+  // per-head scales multiply in inside the kernel, per kv head
+  p.k_scales = fp8 ? pool->k_scales : nullptr;
+  p.v_scales = fp8 ? pool->v_scales : nullptr;
+  p.q_mult = scale * (fp8 && !p.k_scales ? pool->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_mult = fp8 && !p.v_scales ? pool->v_scale : 1.0f;
   return from_cuda(
       pkv::launch_prefill(p, k_pool, v_pool, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -436,12 +478,18 @@ pkv_status pkv_get_device_error(int32_t* code, void* stream) {
   pkv_status st = device_info(&dev);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the landing slot is shared by the host threads that read the word
+  static std::mutex m;
+  std::lock_guard<std::mutex> lock(m);
   int32_t v = 0;
-  const int32_t zero = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
-  if (cudaMemcpyFromSymbol(&v, g_pkv_device_error, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
-  if (cudaMemcpyToSymbol(g_pkv_device_error, &zero, sizeof(zero)) != cudaSuccess)
+  take_error_kernel<<<1, 1, 0, s>>>(dev->err, dev->taken);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, dev->taken, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = e;
     return PKV_ERR_CUDA;
+  }
   *code = v;
   return PKV_OK;
 }

@@ -95,6 +95,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Wait for phase `parity` of `bar` whatever the abort flag says, giving up
+// after `limit` cycles.  A CTA that stops early uses it to let the copies and
+// tensor-core operations it has already issued land before it leaves (its
+// shared memory must not be released under them).  Returns false if it gave
+// up (the timeout is then recorded).
+__device__ __forceinline__ bool mbar_drain_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                long long limit = kWaitLimitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) {
+      record_error(err, kDevTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// mbar_wait_bounded for a whole warp: every lane waits, and the result is
+// true only if every lane saw the phase, so that the warp takes the same
+// branch afterwards (lanes poll separately and may see the abort flag at
+// different times).
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                  volatile int* abort_flag) {
+  const bool ok = mbar_wait_bounded(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---- bulk (TMA engine) copies ----------------------------------------------
 // Order earlier generic-proxy shared-memory accesses before later async-proxy
 // ones (a buffer is rewritten by a bulk copy after threads read it).

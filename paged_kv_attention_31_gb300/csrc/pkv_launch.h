@@ -10,6 +10,8 @@
 #include <mutex>
 #include <utility>
 
+#include "../../include/pkv.h"
+
 namespace pkv {
 
 // Launch with programmatic stream serialization: the kernel may start while
@@ -103,7 +105,11 @@ struct PrefillParams {
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
   int32_t max_blocks, num_blocks, num_q_tokens;
   int32_t tiles_per_seq;        // ceil(max_q_len * G / 128)
-  float q_mult;                 // scale * log2(e)
+  float q_mult;                 // scale * k_scale * log2(e) (k_scale: FP8 per tensor, else 1)
+  float v_mult;                 // v_scale (FP8 per tensor) or 1
+  const float* k_scales;        // optional per-kv-head FP8 scales, multiplied in per head
+  const float* v_scales;
+  int32_t fp8;                  // the pools hold E4M3 codes
 };
 
 // Split plan shared by the host (workspace sizing) and the kernels.
@@ -152,5 +158,13 @@ cudaError_t launch_decode_mma(const DecodeParams& p, bool fp8, int num_sms, cuda
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, int num_sms, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
                            int num_sms, cudaStream_t stream);
+
+// Host validation shared by the decode entry points (pkv_api.cu): the status
+// a decode call reports for these arguments before its workspace is looked at.
+pkv_status decode_args_status(const void* q, const void* k_pool, const void* v_pool,
+                              const pkv_pool_desc* pool, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                              float scale, int32_t partition_tokens, const void* out);
 
 }  // namespace pkv

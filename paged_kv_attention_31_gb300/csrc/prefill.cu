@@ -49,8 +49,6 @@ namespace {
 constexpr int kM = 128;          // query rows per tile
 constexpr int kNK = 128;         // keys per block
 constexpr int kTiles = 2;        // query tiles per CTA
-constexpr int kStagesK = 2;      // K ring depth (key blocks)
-constexpr int kStagesV = 2;      // V ring depth (key blocks)
 constexpr int kSoftmaxThreads = 128 * kTiles;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;   // warp 8: issues every tcgen05.mma
 constexpr int kKLoadWarp = kMmaWarp + 1;         // warp 9: TMA of Q and of the K ring
@@ -59,8 +57,6 @@ constexpr int kThreads = kSoftmaxThreads + 3 * 32;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S (then P) of tile t at 128 t, O of tile t at 256 + D t
 constexpr uint32_t kColS = 0, kColO = 256;
-// barriers: q, k[SK], kfree[SK], v[SV], vfree[SV], s[tiles], p[tiles], o[tiles]
-constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles;
 // CTA order: end positions of up to kMaxRankGroups (sequence, tile pair) groups
 constexpr int kMaxRankGroups = 256;
 // The 128-byte-swizzled tiles need a 1024-aligned base; dynamic shared memory
@@ -68,17 +64,32 @@ constexpr int kMaxRankGroups = 256;
 constexpr int kMaxPad = 1024 - 128;
 
 // Shared memory layout for head_dim D (offsets from a 1024-aligned base).
-// Rows of Q, K and V are split into D/64 halves of 64 bf16 (128 bytes, one
-// swizzle atom): a tile is [half][rows][128 B].
-template <int D>
+// Rows of Q, K and V are split into D/64 halves of 64 16-bit values (128
+// bytes, one swizzle atom): a tile is [half][rows][128 B].  bf16 pools: K and
+// V stream by TMA straight into 2-stage rings of such blocks.  FP8 pools: the
+// TMA lands each key block's E4M3 codes, row-major [key][D], in a 2-stage raw
+// ring; a converter warp turns them into f16 in a 1-stage K (V) block of the
+// same swizzled layout.
+template <int D, bool FP8>
 struct PfLayout {
   static constexpr int kHalves = D / 64;
+  static constexpr int kStagesK = FP8 ? 1 : 2;               // K operand stages (key blocks)
+  static constexpr int kStagesV = FP8 ? 1 : 2;               // V operand stages
+  static constexpr int kRawStages = FP8 ? 2 : 0;             // FP8 code stages, each of K and V
   static constexpr int kQBytes = kHalves * kM * 128;         // per tile
   static constexpr int kKVStageBytes = kHalves * kNK * 128;  // one key block of K or V
+  static constexpr int kRawBytes = kNK * D;                  // one key block of FP8 codes
+  // barriers: q, k[SK], kfree[SK], v[SV], vfree[SV], s[tiles], p[tiles],
+  // o[tiles], drain (the MMA warp's last commit after an abort); FP8 also
+  // qc (Q converted), kraw[R], vraw[R] (code blocks landed)
+  static constexpr int kNumBars =
+      1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles + 1 + (FP8 ? 1 + 2 * kRawStages : 0);
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTiles * kQBytes;
   static constexpr int kOffV = kOffK + kStagesK * kKVStageBytes;
-  static constexpr int kOffBar = kOffV + kStagesV * kKVStageBytes;
+  static constexpr int kOffRawK = kOffV + kStagesV * kKVStageBytes;
+  static constexpr int kOffRawV = kOffRawK + kRawStages * kRawBytes;
+  static constexpr int kOffBar = kOffRawV + kRawStages * kRawBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRank = kOffMisc + 16;
   static constexpr int kSmemBytes = kOffRank + 4 * kMaxRankGroups + kMaxPad;
@@ -227,22 +238,44 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+// Instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1), A and B
+// both bf16 (bits 7-9 and 10-12 = 1) or both f16 (= 0), B K-major or
+// MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_kind(int M, int N, bool b_mn_major, bool f16) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | (b_mn_major ? (1u << 16) : 0u) |
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Four E4M3 codes (bytes 0..3 of w) -> f16x2 (b0, b1) and (b2, b3), exact
+// (every E4M3 value is a normal f16); the lower byte lands in the lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // The register file is handed out per group of four warps, so the 11-warp
 // CTA is budgeted as 12 warps: at most 168 registers per thread.
-template <int D>
+//
+// FP8 pools (FP8 = true): tm_k / tm_v map the E4M3 pools (unswizzled page
+// boxes); each loader warp converts its blocks to f16 (exact) and both
+// products run as kind::f16 MMAs on f16 operands: Q is converted in place to
+// f16 by the softmax threads, each row first multiplied by an exact power of
+// two 2^k that puts its largest |q| in [2^15, 2^16) (the row's scores are
+// multiplied by 2^-k), and P is written to TMEM as f16.  k_scale multiplies
+// the scores, v_scale the output (per tensor, or per kv head).
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   constexpr int kD = D;
-  using Lay = PfLayout<D>;
+  using Lay = PfLayout<D, FP8>;
   constexpr int kHalves = Lay::kHalves, kQBytes = Lay::kQBytes;
-  constexpr int kKVStageBytes = Lay::kKVStageBytes;
+  constexpr int kKVStageBytes = Lay::kKVStageBytes, kRawBytes = Lay::kRawBytes;
+  constexpr int kStagesK = Lay::kStagesK, kStagesV = Lay::kStagesV;
   constexpr int kOffQ = Lay::kOffQ, kOffK = Lay::kOffK, kOffV = Lay::kOffV;
   constexpr int kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffRank = Lay::kOffRank;
   pdl_wait();  // inputs written by earlier kernels of the stream are visible
@@ -323,6 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_s = bar_vfree + kStagesV;         // [kTiles] S_t of the next block ready
   uint64_t* bar_p = bar_s + kTiles;               // [kTiles] P_t written (4 warps)
   uint64_t* bar_o = bar_p + kTiles;               // [kTiles] last PV of tile t done (one phase)
+  uint64_t* bar_drain = bar_o + kTiles;           // every issued MMA done (after an abort)
+  // FP8 only: Q converted to f16 (8 softmax warps), code blocks landed
+  uint64_t* bar_qc = bar_drain + 1;
+  uint64_t* bar_kraw = bar_qc + 1;                // [kRawStages]
+  uint64_t* bar_vraw = bar_kraw + Lay::kRawStages;  // [kRawStages]
+  uint8_t* sRawK = smem + Lay::kOffRawK;
+  uint8_t* sRawV = smem + Lay::kOffRawV;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -351,6 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 4);
       mbar_init(&bar_o[t], 1);
+    }
+    mbar_init(bar_drain, 1);
+    if constexpr (FP8) {
+      mbar_init(bar_qc, 8);
+      for (int i = 0; i < Lay::kRawStages; ++i) {
+        mbar_init(&bar_kraw[i], 1);
+        mbar_init(&bar_vraw[i], 1);
+      }
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -392,22 +440,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // a loader streams blocks 0 .. nblk-1 into its ring; block b reuses the
-  // stage of block b - stages once `freed` says the MMAs reading it are done
+  // stage of block b - stages once `freed` says the MMAs reading it are done.
+  // If a wait gives up it stops issuing; either way it returns only after
+  // the copies it issued into the ring have landed (on the normal path the
+  // MMA warp has already seen them all, so this returns at once).
   auto run_loader = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* freed,
                         int stages) {
     constexpr int kLead = 3;  // page ids are read kLead blocks ahead
     int ids[kLead];
 #pragma unroll
     for (int k = 0; k < kLead; ++k) ids[k] = fetch_ids(k);
+    int issued = 0;
     for (int b = 0; b < nblk; ++b) {
-      if (b >= stages)
-        mbar_wait_bounded(&freed[b % stages], uint32_t((b - stages) / stages) & 1, p.err,
-                          abort_flag);
+      if (b >= stages && !warp_wait_bounded(&freed[b % stages],
+                                            uint32_t((b - stages) / stages) & 1, p.err,
+                                            abort_flag))
+        break;
       load_blk(map, ring, full, stages, b, ids[0]);
+      issued = b + 1;
 #pragma unroll
       for (int k = 0; k + 1 < kLead; ++k) ids[k] = ids[k + 1];
       ids[kLead - 1] = fetch_ids(b + kLead);
     }
+    if (lane == 0)
+      for (int b = max(0, issued - stages); b < issued; ++b)
+        mbar_drain_wait(&full[b % stages], uint32_t(b / stages) & 1, p.err);
+    __syncwarp();
+  };
+
+  // ---- FP8 pools: code blocks by TMA, converted to f16 operand blocks ----
+  // TMA of one key block's code pages (row-major [key][D]) into raw stage
+  // blk % kRawStages (whole loader warp)
+  auto load_raw = [&](const CUtensorMap* map, uint8_t* raw, uint64_t* bars, int blk, int ids) {
+    const int st = blk % Lay::kRawStages;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], kRawBytes);
+#pragma unroll
+    for (int i = 0; i < kNK / 16; ++i) {  // at most 8 pages per block (block_size >= 16)
+      const int pid = __shfl_sync(0xffffffffu, ids, i);
+      if (lane == 0 && i < pages_per_blk)
+        tma_load_4d(raw + st * kRawBytes + i * P * kD, map, 0, 0, h, pid, &bars[st]);
+    }
+  };
+  // the codes of one key block -> f16 in the swizzled operand layout (the
+  // one a 128-byte-swizzled TMA box of 16-bit values gives); key rows from
+  // zero_from on are written as zeros: slots past the sequence may hold NaN
+  // codes, and 0 * V must stay 0 in the PV product
+  auto convert_blk = [&](const uint8_t* raw, uint8_t* dst, int zero_from) {
+    constexpr int kGroups = kD / 16;  // 16-code groups per key row
+    for (int i = lane; i < kNK * kGroups; i += 32) {
+      const int r = i / kGroups, g = i - r * kGroups;
+      uint4 u = *reinterpret_cast<const uint4*>(raw + r * kD + g * 16);
+      if (r >= zero_from) u = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t f[8];
+      e4m3x4_to_f16x2(u.x, f[0], f[1]);
+      e4m3x4_to_f16x2(u.y, f[2], f[3]);
+      e4m3x4_to_f16x2(u.z, f[4], f[5]);
+      e4m3x4_to_f16x2(u.w, f[6], f[7]);
+      // values 16g .. 16g + 15: half 16g / 64, 16-byte chunks c and c + 1
+      const int dh = (16 * g) / 64, c = ((16 * g) % 64) / 8;
+      uint8_t* row = dst + dh * (kNK * 128) + r * 128;
+      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<uint4*>(row + (((c + 1) ^ (r & 7)) << 4)) =
+          make_uint4(f[4], f[5], f[6], f[7]);
+    }
+  };
+  // a converter warp keeps kRawStages code blocks in flight; block b is
+  // converted into operand stage b % stages once `freed` says the MMAs that
+  // read its previous block are done, and `ready` then signals the MMA warp.
+  // If a wait gives up it stops; either way it returns only after its code
+  // copies in flight have landed.
+  auto run_converter = [&](const CUtensorMap* map, uint8_t* raw, uint64_t* raw_full,
+                           uint8_t* ops, uint64_t* ready, uint64_t* freed, int stages) {
+    constexpr int R = Lay::kRawStages;
+    constexpr int kLead = 3;  // page ids are read kLead blocks ahead
+    int ids[kLead];
+#pragma unroll
+    for (int k = 0; k < kLead; ++k) ids[k] = fetch_ids(k);
+    int issued = 0;  // code blocks whose copies were issued
+    auto issue_next = [&]() {
+      load_raw(map, raw, raw_full, issued, ids[0]);
+#pragma unroll
+      for (int k = 0; k + 1 < kLead; ++k) ids[k] = ids[k + 1];
+      ids[kLead - 1] = fetch_ids(issued + kLead);
+      ++issued;
+    };
+    while (issued < R && issued < nblk) issue_next();
+    for (int b = 0; b < nblk; ++b) {
+      if (!warp_wait_bounded(&raw_full[b % R], uint32_t(b / R) & 1, p.err, abort_flag)) break;
+      if (b >= stages && !warp_wait_bounded(&freed[b % stages],
+                                            uint32_t((b - stages) / stages) & 1, p.err,
+                                            abort_flag))
+        break;
+      convert_blk(raw + (b % R) * kRawBytes, ops + (b % stages) * kKVStageBytes, L - b * kNK);
+      // the MMAs (async proxy) read the block next, and the next code copy
+      // (async proxy) rewrites the raw stage just read
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[b % stages]);
+      if (issued < nblk) issue_next();
+    }
+    if (lane == 0)
+      for (int b = max(0, issued - R); b < issued; ++b)
+        mbar_drain_wait(&raw_full[b % R], uint32_t(b / R) & 1, p.err);
+    __syncwarp();
   };
 
   if (warp == kKLoadWarp) {
@@ -419,12 +554,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sQ + t * kQBytes + dh * (kM * 128), &tm_q, dh * 64, 0, h,
                       q0 + tokA + t * TQ, bar_q);
     }
-    run_loader(&tm_k, sK, bar_k, bar_kfree, kStagesK);
+    if constexpr (FP8)
+      run_converter(&tm_k, sRawK, bar_kraw, sK, bar_k, bar_kfree, kStagesK);
+    else
+      run_loader(&tm_k, sK, bar_k, bar_kfree, kStagesK);
+    if (lane == 0) mbar_drain_wait(bar_q, 0, p.err);  // Q landed (normally seen long ago)
+    __syncwarp();
   } else if (warp == kVLoadWarp) {
-    run_loader(&tm_v, sV, bar_v, bar_vfree, kStagesV);
+    if constexpr (FP8)
+      run_converter(&tm_v, sRawV, bar_vraw, sV, bar_v, bar_vfree, kStagesV);
+    else
+      run_loader(&tm_v, sV, bar_v, bar_vfree, kStagesV);
   } else if (warp == kMmaWarp) {
-    constexpr uint32_t kIdescS = idesc_bf16(kM, kNK, false);
-    constexpr uint32_t kIdescO = idesc_bf16(kM, kD, true);
+    constexpr uint32_t kIdescS = idesc_f16_kind(kM, kNK, false, FP8);
+    constexpr uint32_t kIdescO = idesc_f16_kind(kM, kD, true, FP8);
     auto issue_s = [&](int t, int blk) {  // lane 0: S_t of block blk
       const uint32_t qa = smem_u32(sQ + t * kQBytes);
       const uint32_t ka = smem_u32(sK + (blk % kStagesK) * kKVStageBytes);
@@ -448,13 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) mma_commit(&bar_o[t]);
     };
     auto wait_k = [&](int b) {
-      mbar_wait_bounded(&bar_k[b % kStagesK], uint32_t(b / kStagesK) & 1, p.err, abort_flag);
+      return warp_wait_bounded(&bar_k[b % kStagesK], uint32_t(b / kStagesK) & 1, p.err,
+                               abort_flag);
     };
 
-    mbar_wait_bounded(bar_q, 0, p.err, abort_flag);
-    if (nblk > 0) {
-      wait_k(0);
-      if (lane == 0) {
+    // `alive` turns false when a wait gives up: no further MMA is issued.
+    // FP8: Q is read once the softmax warps have converted it to f16.
+    bool alive = warp_wait_bounded(FP8 ? bar_qc : bar_q, 0, p.err, abort_flag);
+    if (alive && nblk > 0) {
+      alive = wait_k(0);
+      if (alive && lane == 0) {
         tc_fence_after();
         if (nb0 > 0) issue_s(0, 0);
         if (nb1 > 0) issue_s(1, 0);
@@ -462,12 +608,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    for (int j = 0; j < nblk; ++j) {
+    for (int j = 0; alive && j < nblk; ++j) {
       const int sv = j % kStagesV;
       // V_j landed; rows past the sequence end may hold never-written slots:
       // zero them so that 0 * V stays 0 in the PV product
-      mbar_wait_bounded(&bar_v[sv], uint32_t(j / kStagesV) & 1, p.err, abort_flag);
-      if (j * kNK + kNK > L) {
+      if (!warp_wait_bounded(&bar_v[sv], uint32_t(j / kStagesV) & 1, p.err, abort_flag)) {
+        alive = false;
+        break;
+      }
+      if (!FP8 && j * kNK + kNK > L) {  // (FP8: the converter wrote those rows as zeros)
         const int first = max(0, L - j * kNK);
         for (int i = lane; i < (kNK - first) * 8 * kHalves; i += 32) {
           const int r = first + i / (8 * kHalves), dh = (i / 8) % kHalves, chunk = i % 8;
@@ -485,7 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < kTiles; ++t) {
         const int nbt = t == 0 ? nb0 : nb1;
         if (j >= nbt) continue;
-        mbar_wait_bounded(&bar_p[t], uint32_t(j) & 1, p.err, abort_flag);
+        if (!warp_wait_bounded(&bar_p[t], uint32_t(j) & 1, p.err, abort_flag)) {
+          alive = false;
+          break;
+        }
         if (lane == 0) {
           tc_fence_after();
           issue_pv(t, j, j == nbt - 1);
@@ -493,17 +645,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (j + 1 < nbt) {
           if (!k_ready) {
-            wait_k(j + 1);
+            if (!wait_k(j + 1)) {
+              alive = false;
+              break;
+            }
             k_ready = true;
           }
           if (lane == 0) issue_s(t, j + 1);
           __syncwarp();
         }
       }
+      if (!alive) break;
       // stage release: V_j after both tiles' PV, K_{j+1} after both tiles' S
       if (lane == 0) {
         mma_commit(&bar_vfree[sv]);
         if (j + 1 < nblk) mma_commit(&bar_kfree[(j + 1) % kStagesK]);
+      }
+      __syncwarp();
+    }
+    if (!alive) {
+      // every MMA this thread issued completes before TMEM is released (a
+      // commit arrives once all of the thread's earlier MMAs are done)
+      if (lane == 0) {
+        mma_commit(bar_drain);
+        mbar_drain_wait(bar_drain, 0, p.err);
       }
       __syncwarp();
     }
@@ -517,13 +682,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = (row / G) < (t == 0 ? ntok0 : ntok1);
     const int pos = row_valid ? L - C + tok : -1;  // keys 0 .. pos are visible
     const int minpos = L - C + tokA + t * TQ;      // first token of the tile
-    const float qm = p.q_mult;                     // scale * log2(e) > 0
+    float qm = p.q_mult;                           // scale * k_scale * log2(e) > 0
     float m_used = -INFINITY, l_sum = 0.f;
     const int nb = t == 0 ? nb0 : nb1;
 
-    for (int j = 0; j < nb; ++j) {
-      mbar_wait_bounded(&bar_s[t], uint32_t(j) & 1, p.err, abort_flag);
-      __syncwarp();  // lanes leave the polling loop separately; the TMEM loads are collective
+    bool alive = true;  // false once a wait gives up: no more TMEM work, no stores
+    if constexpr (FP8) {
+      if (p.k_scales) qm *= __ldg(p.k_scales + h);
+      // This thread's row of Q to f16 in place, times 2^k with k = 15 -
+      // floor(log2 max|q|) (clamped to [-126, 64], so that 2^k and the row's
+      // score multiplier qm * 2^-k stay normal floats): f16 then holds every
+      // value of the row within 2^29 of its largest exactly.
+      alive = warp_wait_bounded(bar_q, 0, p.err, abort_flag);
+      if (alive) {
+        uint8_t* const qrow = sQ + t * kQBytes + row * 128;
+        float amax = 0.f;
+#pragma unroll
+        for (int dh = 0; dh < kHalves; ++dh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u =
+                *reinterpret_cast<const uint4*>(qrow + dh * (kM * 128) + ((c ^ (row & 7)) << 4));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = bf16x2_to_float2(w[i]);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+        const int e = int((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // -127 if subnormal
+        const int k = amax > 0.f ? max(-126, min(64, 15 - e)) : 0;
+        const float up = __uint_as_float(uint32_t(127 + k) << 23);
+        qm *= __uint_as_float(uint32_t(127 - k) << 23);
+#pragma unroll
+        for (int dh = 0; dh < kHalves; ++dh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* at =
+                reinterpret_cast<uint4*>(qrow + dh * (kM * 128) + ((c ^ (row & 7)) << 4));
+            const uint4 u = *at;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = bf16x2_to_float2(w[i]);
+              const __half2 hv = __floats2half2_rn(f.x * up, f.y * up);  // exact products
+              o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            *at = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        fence_proxy_async_smem();  // the S MMAs (async proxy) read Q next
+      }
+      __syncwarp();
+      if (alive && lane == 0) mbar_arrive(bar_qc);
+    }
+    for (int j = 0; alive && j < nb; ++j) {
+      // lanes leave the polling loop separately; the TMEM loads are
+      // collective, and the warp takes one branch on the result
+      if (!warp_wait_bounded(&bar_s[t], uint32_t(j) & 1, p.err, abort_flag)) {
+        alive = false;
+        break;
+      }
       tc_fence_after();
       const int kbase = j * kNK;
       const bool diag = kbase + kNK - 1 > minpos;   // causal mask inside this block
@@ -571,8 +790,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x2 = __ffma2_rn(make_float2(sv[c + i], sv[c + i + 1]), qm2, nm2);
           const float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
           acc2[(i >> 1) & 1] = __fadd2_rn(acc2[(i >> 1) & 1], e2);
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
-          pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          if constexpr (FP8) {  // the PV product's operands are f16
+            const __half2 ph = __floats2half2_rn(e2.x, e2.y);
+            pw[i / 2] = *reinterpret_cast<const uint32_t*>(&ph);
+          } else {
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
+            pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
         }
         tmem_st16_async(tmem + lane_base + colS + c / 2, pw);
       }
@@ -600,12 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O / l -> bf16 ----------------------------------------------------
-    if (nb > 0) {
-      // the last PV's commit also covers every earlier MMA of the producer
-      mbar_wait_bounded(&bar_o[t], 0, p.err, abort_flag);
-      __syncwarp();
+    // the last PV's commit also covers every earlier MMA of the producer
+    if (nb > 0 && alive && warp_wait_bounded(&bar_o[t], 0, p.err, abort_flag)) {
       tc_fence_after();
-      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      // v_scale (FP8 pools; 1 otherwise) applied once, with the normalisation
+      const float vm = p.v_scales ? p.v_mult * __ldg(p.v_scales + h) : p.v_mult;
+      const float inv = l_sum > 0.f ? vm / l_sum : 0.f;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
                            (size_t(q0 + tok) * p.num_q_heads + size_t(h) * G + (row % G)) * kD;
 #pragma unroll 1
@@ -639,10 +863,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const void* v_pool,
                              cudaStream_t stream) {
-  using Lay = PfLayout<D>;
+  using Lay = PfLayout<D, FP8>;
   const int G = p.num_q_heads / p.num_kv_heads;
   if (G < 1 || kM % G != 0 || kNK % p.block_size != 0) return cudaErrorNotSupported;
   if (p.num_blocks >= (1 << 30)) return cudaErrorInvalidValue;
@@ -653,20 +877,33 @@ cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const v
   if (!make_map_4d(&tq, kBf16, p.q, D, G, Hkv, uint64_t(p.num_q_tokens), D * E, G * D * E,
                    Hkv * G * D * E, 64, uint32_t(G), 1, uint32_t(kM / G)))
     return cudaErrorInvalidValue;
-  // pools [nb][Hkv][P][D] with box (64, P, 1, 1): one page of one kv head
-  if (!make_map_4d(&tk, kBf16, k_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
-                   Hkv * P * D * E, 64, uint32_t(P), 1, 1))
-    return cudaErrorInvalidValue;
-  if (!make_map_4d(&tv, kBf16, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
-                   Hkv * P * D * E, 64, uint32_t(P), 1, 1))
-    return cudaErrorInvalidValue;
+  if constexpr (FP8) {
+    // E4M3 pools [nb][Hkv][P][D] bytes with box (D, P, 1, 1): one page of
+    // one kv head, unswizzled (row-major [key][D] in shared memory)
+    const auto kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map_4d(&tk, kU8, k_pool, D, P, Hkv, uint64_t(p.num_blocks), D, P * D, Hkv * P * D,
+                     uint32_t(D), uint32_t(P), 1, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    if (!make_map_4d(&tv, kU8, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D, P * D, Hkv * P * D,
+                     uint32_t(D), uint32_t(P), 1, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    // pools [nb][Hkv][P][D] with box (64, P, 1, 1): one page of one kv head
+    if (!make_map_4d(&tk, kBf16, k_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
+                     Hkv * P * D * E, 64, uint32_t(P), 1, 1))
+      return cudaErrorInvalidValue;
+    if (!make_map_4d(&tv, kBf16, v_pool, D, P, Hkv, uint64_t(p.num_blocks), D * E, P * D * E,
+                     Hkv * P * D * E, 64, uint32_t(P), 1, 1))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = prefill_kernel<D, FP8>;
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   e = once_per_device(configured, dev, [&] {
-    return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Lay::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
@@ -675,7 +912,7 @@ cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const v
       int64_t((p.tiles_per_seq + kTiles - 1) / kTiles) * p.num_kv_heads * p.num_seqs;
   if (ctas > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   const dim3 grid{static_cast<unsigned>(ctas)};
-  e = launch_pdl(prefill_kernel<D>, grid, dim3(kThreads), Lay::kSmemBytes, stream, tq, tk, tv, p);
+  e = launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, stream, tq, tk, tv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -685,8 +922,12 @@ cudaError_t launch_prefill_d(const PrefillParams& p, const void* k_pool, const v
 cudaError_t launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool,
                            int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  if (p.head_dim == 128) return launch_prefill_d<128>(p, k_pool, v_pool, stream);
-  if (p.head_dim == 64) return launch_prefill_d<64>(p, k_pool, v_pool, stream);
+  if (p.head_dim == 128)
+    return p.fp8 ? launch_prefill_d<128, true>(p, k_pool, v_pool, stream)
+                 : launch_prefill_d<128, false>(p, k_pool, v_pool, stream);
+  if (p.head_dim == 64)
+    return p.fp8 ? launch_prefill_d<64, true>(p, k_pool, v_pool, stream)
+                 : launch_prefill_d<64, false>(p, k_pool, v_pool, stream);
   return cudaErrorNotSupported;
 }
 

@@ -1,54 +1,15 @@
-"""GPU-test helpers: device inputs from the seeded generator, and the
-oracle-side state of one (sequence, kv head) rebuilt on the host from the
-same generator (never from the CUDA path).
+"""GPU-test helpers: the oracle-side state of one (sequence, kv head)
+rebuilt on the host from the seeded generator (never from the CUDA path),
+the tolerance check, and the device inputs (from device_inputs.py).
 """
 import numpy as np
 import torch
 
 import oracle
-import paged_kv_attention_31_gb300 as pkv
 import workloads as W
+from device_inputs import device_pools, device_step_inputs  # noqa: F401  (re-exported)
 
 BF16_MAX_ABS, BF16_MEAN_ABS, FP8_MAX_ABS = 2e-2, 2e-3, 6e-2
-
-
-def device_pools(w: W.Workload, device="cuda"):
-    """Pools holding the generator's values (FP8: encoded by pkv_kv_append)."""
-    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
-    if w.kv_dtype == "bf16":
-        k = W.fill_pool_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, "k")
-        v = W.fill_pool_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, "v")
-        return k, v
-    k = torch.empty(shape, dtype=torch.uint8, device=device)
-    v = torch.empty(shape, dtype=torch.uint8, device=device)
-    ks, vs = w.scale_tensors(device)
-    per_page = w.num_kv_heads * w.block_size * w.head_dim
-    chunk = max(1, (1 << 25) // per_page)
-    P = w.block_size
-    for start in range(0, w.num_blocks, chunk):
-        stop = min(w.num_blocks, start + chunk)
-        ids = np.arange(start, stop)
-        rows = lambda x: x.permute(0, 2, 1, 3).reshape(-1, w.num_kv_heads, w.head_dim).contiguous()
-        kn = rows(w.pool_source("k", ids, device))
-        vn = rows(w.pool_source("v", ids, device))
-        slots = torch.arange(start * P, stop * P, dtype=torch.int64, device=device)
-        pkv.kv_append(kn, vn, slots, k, v, w.k_scale, w.v_scale, k_scales=ks, v_scales=vs)
-    return k, v
-
-
-def device_step_inputs(w: W.Workload, device="cuda"):
-    d = {}
-    d["q"] = w.q_decode(device)
-    d["k_new"], d["v_new"] = w.kv_new(device)
-    d["slots"] = torch.from_numpy(w.append_slot_mapping()).to(device)
-    d["block_tables"] = torch.from_numpy(w.block_tables).to(device)
-    d["context_lens"] = torch.from_numpy(w.context_lens).to(device)
-    if w.num_prefill:
-        d["q_prefill"] = w.q_prefill(device)
-        d["cu_seqlens_q"] = torch.from_numpy(w.cu_seqlens_q()).to(device)
-        d["prefill_block_tables"] = torch.from_numpy(w.prefill_block_tables).to(device)
-        d["prefill_context_lens"] = torch.from_numpy(w.prefill_context_lens).to(device)
-    return d
 
 
 def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None):
@@ -83,19 +44,24 @@ def host_head_pools(w: W.Workload, page_ids, h: int, k_new_h=None, v_new_h=None)
     return kp, vp
 
 
-def oracle_decode_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
-    """fp64 oracle output [G, D] of decode sequence s, q heads of kv head h."""
+def oracle_decode_rows(w: W.Workload, s: int, h: int, kv_new_h=None, q_host=None,
+                       scale=None):
+    """fp64 oracle output [G, D] of decode sequence s, q heads of kv head h.
+
+    q_host (bf16 CPU tensor [B, Hq, D]) and scale replace the workload's own
+    q and softmax scale when given."""
     L = int(w.context_lens[s])
     P = w.block_size
     npg = (L + P - 1) // P
     pages = w.block_tables[s, :npg]
     kp, vp = host_head_pools(w, pages, h, *(kv_new_h or (None, None)))
     G = w.group
-    q = W.bf16_bits(w.q_decode()[s, h * G:(h + 1) * G, :])[None]
+    qa = w.q_decode() if q_host is None else q_host
+    q = W.bf16_bits(qa[s, h * G:(h + 1) * G, :])[None]
     table = np.arange(max(npg, 1), dtype=np.int32)[None]
     ks, vs = w.head_scales(h)
-    out = oracle.paged_attention(q, kp, vp, table, np.array([L], np.int32), w.scale,
-                                 w.kv_dtype, ks, vs)
+    out = oracle.paged_attention(q, kp, vp, table, np.array([L], np.int32),
+                                 w.scale if scale is None else scale, w.kv_dtype, ks, vs)
     return out[0]
 
 
@@ -111,8 +77,9 @@ def oracle_prefill_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
     cu = w.cu_seqlens_q()
     q = W.bf16_bits(w.q_prefill()[cu[s]:cu[s + 1], h * G:(h + 1) * G, :])
     table = np.arange(max(npg, 1), dtype=np.int32)[None]
+    ks, vs = w.head_scales(h)
     out = oracle.paged_prefill(q, np.array([0, C], np.int32), kp, vp, table,
-                               np.array([L], np.int32), w.scale)
+                               np.array([L], np.int32), w.scale, w.kv_dtype, ks, vs)
     return out
 
 

@@ -86,9 +86,13 @@ def test_argument_validation_before_any_cuda_call(lib):
     assert lib.pkv_paged_attention(*args(3)) == 1
     assert lib.pkv_paged_attention(*args(4, part=24)) == 1     # not a multiple of block size
     assert lib.pkv_paged_attention(*args(4, ws=ctypes.c_void_p(272))) == 3  # misaligned workspace
-    # prefill: FP8 pools are not built
-    d8 = _desc(kv_dtype=1)
+    # prefill over an FP8 pool: the pool's scales are checked, and a group
+    # size that does not divide 128 is not built
+    d8 = _desc(kv_dtype=1, k_scale=0.0)
     assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d8), one, 4, one, 1, 4, 16, 16,
+                                 0.1, one, z) == 1
+    d8 = _desc(kv_dtype=1, k_scale=0.01, v_scale=0.02)
+    assert lib.pkv_paged_prefill(one, one, one, one, ctypes.byref(d8), one, 4, one, 1, 6, 16, 16,
                                  0.1, one, z) == 2
 
 
@@ -130,3 +134,19 @@ def test_self_test_validation_before_any_cuda_call(lib):
     assert lib.pkv_self_test_bounded_wait(0, out, None) == 1              # limit must be > 0
     assert lib.pkv_self_test_bounded_wait(3_000_000_000, out, None) == 1  # above the kernels' own
     assert lib.pkv_self_test_bounded_wait(1000, ctypes.c_void_p(258), None) == 1  # misaligned
+
+
+@pytest.mark.parametrize("kw,nseq,status", [
+    (None, 0, 1),                       # no pool descriptor, even with nothing to do
+    (dict(head_dim=96), 4, 2), (dict(block_size=8), 4, 2), (dict(kv_dtype=7), 4, 1),
+    (dict(num_blocks=0), 0, 1), (dict(), 0, 0),
+    (dict(), -1, 1)])
+def test_noalloc_reports_the_same_status_as_the_workspace_entry_point(lib, kw, nseq, status):
+    # both decode entry points run the same host checks in the same order
+    # (no CUDA call is reached for any of these arguments)
+    z = ctypes.c_void_p(0)
+    d = None if kw is None else _desc(**kw)
+    dp = ctypes.byref(d) if d is not None else ctypes.POINTER(pkv.PoolDesc)()
+    a = lib.pkv_paged_attention(z, z, z, dp, z, 4, z, nseq, 4, 64, 0.1, 0, z, 0, z, z)
+    b = lib.pkv_paged_attention_noalloc(z, z, z, dp, z, 4, z, nseq, 4, 64, 0.1, 0, z, z)
+    assert a == b == status

@@ -1,6 +1,9 @@
 """Chunked-prefill attention (tcgen05 kernel) on the GPU against the oracle.
 
-Tolerance as for bf16 decode: max |err| <= 2e-2, mean |err| <= 2e-3.
+Tolerances as for decode: bf16 pools max |err| <= 2e-2, mean |err| <= 2e-3;
+FP8 pools max |err| <= 6e-2 against the oracle run on the same stored codes
+("TensorRT-LLM框架解析与高性能推理优化实践" §5.3 chunked context over the cache
+that §7.2 stores quantised and dequantises inside attention).
 """
 import numpy as np
 import pytest
@@ -15,22 +18,28 @@ pytestmark = pytest.mark.gpu
 
 
 def _prefill(w, d, kp, vp, append=True):
+    ks, vs = w.scale_tensors(d["q_prefill"].device)
     if append:
-        pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp)
+        pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale,
+                      k_scales=ks, v_scales=vs)
     return pkv.paged_prefill(d["q_prefill"], d["cu_seqlens_q"], kp, vp,
                              d["prefill_block_tables"], d["prefill_context_lens"],
-                             int(w.prefill_chunk_lens.max()), w.scale)
+                             int(w.prefill_chunk_lens.max()), w.scale, k_scale=w.k_scale,
+                             v_scale=w.v_scale, k_scales=ks, v_scales=vs)
 
 
 def _check(w, out, seqs=None, heads=None):
+    """Rows against the fp64 oracle: bf16 pools at max |err| <= 2e-2 and mean
+    <= 2e-3, FP8 pools at max |err| <= 6e-2 (the oracle reads the same codes)."""
     G = w.group
     cu = w.cu_seqlens_q()
     kn, vn = w.kv_new()
+    fp8 = w.kv_dtype == "fp8_e4m3"
     for s in (range(w.num_prefill) if seqs is None else seqs):
         for h in (range(w.num_kv_heads) if heads is None else heads):
             kv = (W.bf16_bits(kn[:, h, :]), W.bf16_bits(vn[:, h, :]))
             want = oracle_prefill_rows(w, s, h, kv)
-            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, False,
+            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, fp8,
                          f"{w.name} s={s} h={h}")
 
 
@@ -189,3 +198,108 @@ def test_full_size_mixed_step_sampled():
         h = int(rng.integers(0, w.num_kv_heads))
         assert_close(out_d[s, h * G:(h + 1) * G], oracle_decode_rows(w, s, h), False,
                      f"mixed decode s={s}")
+
+
+# ---- FP8 pools -------------------------------------------------------------------
+@pytest.mark.parametrize("G,P,D", [(1, 16, 128), (2, 32, 128), (4, 32, 128), (8, 64, 128),
+                                   (16, 64, 128), (4, 128, 128), (8, 16, 64), (2, 128, 64),
+                                   (4, 32, 64)])
+@pytest.mark.parametrize("head_scales", [False, True])
+def test_fp8_pool_groups_blocks_and_ragged_chunks(G, P, D, head_scales):
+    priors = [0, 7, 64, 129, 0]
+    chunks = [1, 33, 200, 64, 257]
+    hkv = 2
+    w = W.make_mixed(f"prefill_fp8_G{G}_P{P}_D{D}", 7100 + G + P + D, [40], priors, chunks,
+                     hkv * G, hkv, D, P, kv_dtype="fp8_e4m3")
+    if head_scales:
+        w = W.with_head_scales(w)
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    _check(w, out)
+
+
+def test_fp8_never_written_slots_past_the_end_do_not_leak():
+    # E4M3 NaN codes (both signs) in every slot past each sequence's last token
+    w = W.make_mixed("prefill_fp8_nan_tail", 7234, [30], [5, 70, 300], [50, 27, 130], 32, 8, 128,
+                     32, kv_dtype="fp8_e4m3")
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale)
+    P = w.block_size
+    for s in range(w.num_prefill):
+        L = int(w.prefill_context_lens[s])
+        last = int(w.prefill_block_tables[s, (L - 1) // P])
+        off = L % P
+        if off:
+            for pool in (kp, vp):
+                pool[last, :, off:, 0::2] = 0x7F
+                pool[last, :, off:, 1::2] = 0xFF
+    out = _prefill(w, d, kp, vp, append=False)
+    assert pkv.get_device_error() == 0
+    assert torch.isfinite(out.float()).all()
+    _check(w, out)
+
+
+@pytest.mark.parametrize("mult,scale_div", [(2.0 ** 16, 2.0 ** 16), (2.0 ** -20, 2.0 ** -20),
+                                            (300.0, 1.0)])
+def test_fp8_pool_q_far_from_unit_scale(mult, scale_div):
+    # q rows far outside f16's range (or deep in its subnormals), the softmax
+    # scale divided by the same power of two: the per-row power-of-two
+    # scaling before the f16 conversion keeps the scores exact
+    w = W.make_mixed("prefill_fp8_qrange", 7321, [20], [0, 90], [70, 150], 32, 8, 128, 32,
+                     kv_dtype="fp8_e4m3")
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale)
+    q_host = (w.q_prefill().float() * mult).to(torch.bfloat16)
+    scale = w.scale / scale_div
+    out = pkv.paged_prefill(q_host.to("cuda"), d["cu_seqlens_q"], kp, vp,
+                            d["prefill_block_tables"], d["prefill_context_lens"],
+                            int(w.prefill_chunk_lens.max()), scale, k_scale=w.k_scale,
+                            v_scale=w.v_scale)
+    assert pkv.get_device_error() == 0
+    G = w.group
+    cu = w.cu_seqlens_q()
+    kn, vn = w.kv_new()
+    for s in range(w.num_prefill):
+        for h in (0, w.num_kv_heads - 1):
+            kv = (W.bf16_bits(kn[:, h, :]), W.bf16_bits(vn[:, h, :]))
+            want = _oracle_prefill_rows_q(w, s, h, kv, q_host, scale)
+            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, True, f"s={s} h={h}")
+
+
+def _oracle_prefill_rows_q(w, s, h, kv, q_host, scale):
+    """oracle_prefill_rows with q and the softmax scale replaced."""
+    import oracle
+    from tests._gpu_state import host_head_pools
+    L, C, P = int(w.prefill_context_lens[s]), int(w.prefill_chunk_lens[s]), w.block_size
+    npg = (L + P - 1) // P
+    kp, vp = host_head_pools(w, w.prefill_block_tables[s, :npg], h, *kv)
+    G = w.group
+    cu = w.cu_seqlens_q()
+    q = W.bf16_bits(q_host[cu[s]:cu[s + 1], h * G:(h + 1) * G, :])
+    ks, vs = w.head_scales(h)
+    return oracle.paged_prefill(q, np.array([0, C], np.int32), kp, vp,
+                                np.arange(npg, dtype=np.int32)[None], np.array([L], np.int32),
+                                scale, w.kv_dtype, ks, vs)
+
+
+def test_full_size_mixed_step_fp8_sampled():
+    w = W.config("mixed_fp8")
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale)
+    out_d = pkv.paged_attention(d["q"], kp, vp, d["block_tables"], d["context_lens"],
+                                w.max_context_len, w.scale, k_scale=w.k_scale, v_scale=w.v_scale)
+    out_p = _prefill(w, d, kp, vp, append=False)
+    assert pkv.get_device_error() == 0
+    G = w.group
+    rng = np.random.default_rng(6)
+    for s in range(w.num_prefill):
+        _check(w, out_p, seqs=[s], heads=[int(rng.integers(0, w.num_kv_heads))])
+    for s in (0, int(np.argmax(w.context_lens))):
+        h = int(rng.integers(0, w.num_kv_heads))
+        assert_close(out_d[s, h * G:(h + 1) * G], oracle_decode_rows(w, s, h), True,
+                     f"mixed fp8 decode s={s}")

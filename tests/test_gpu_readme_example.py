@@ -1,25 +1,19 @@
-"""The README's Python example, run as written (the block between its
-example markers), so the documented calls stay the library's real API."""
+"""The Python usage example (examples/readme_step.py), run as a script, so
+the documented calls stay the library's real API."""
 import os
-import re
+import runpy
 
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-
-
-def _example() -> str:
-    text = open(os.path.join(ROOT, "README.md"), encoding="utf-8").read()
-    m = re.search(r"<!-- example:begin -->\s*```python\n(.*?)```\s*<!-- example:end -->", text,
-                  re.S)
-    assert m, "README example block not found"
-    return m.group(1)
+EXAMPLE = os.path.join(ROOT, "examples", "readme_step.py")
 
 
 def test_example_is_valid_python():
-    compile(_example(), "README.md example", "exec")
+    with open(EXAMPLE, encoding="utf-8") as f:
+        compile(f.read(), EXAMPLE, "exec")
 
 
 @pytest.mark.gpu
 def test_example_runs():
-    exec(compile(_example(), "README.md example", "exec"), {})
+    runpy.run_path(EXAMPLE, run_name="__main__")

@@ -395,7 +395,7 @@ def with_head_scales(w: Workload) -> Workload:
 
 
 def make_mixed(name, seed, decode_lens, prior_lens, chunk_lens, Hq, Hkv, D, P,
-               max_blocks=None, num_blocks=None) -> Workload:
+               max_blocks=None, num_blocks=None, kv_dtype="bf16") -> Workload:
     """Decode sequences plus prefill chunks appended onto prior contexts."""
     rng = np.random.Generator(np.random.PCG64(seed + 7777))
     decode_lens = np.asarray(decode_lens, np.int32)
@@ -407,8 +407,16 @@ def make_mixed(name, seed, decode_lens, prior_lens, chunk_lens, Hq, Hkv, D, P,
         max_blocks = int(_pages(np.array([int(all_lens.max())]), P)[0])
     tables, nb = _allocate(rng, all_lens, P, max_blocks, num_blocks=num_blocks)
     B = len(decode_lens)
-    return Workload(name, seed, Hq, Hkv, D, P, "bf16", nb, decode_lens,
-                    tables[:B].copy(), pre_lens, chunk_lens, tables[B:].copy())
+    sc = FP8_SCALE if kv_dtype == "fp8_e4m3" else 1.0
+    return Workload(name, seed, Hq, Hkv, D, P, kv_dtype, nb, decode_lens,
+                    tables[:B].copy(), pre_lens, chunk_lens, tables[B:].copy(), sc, sc)
+
+
+def with_fp8_kv(w: Workload) -> Workload:
+    """The same batch (lengths, pages, values) with the KV pool stored as FP8
+    E4M3 codes under the per-tensor scale FP8_SCALE."""
+    return dataclasses.replace(w, name=w.name + "_fp8kv", kv_dtype="fp8_e4m3",
+                               k_scale=FP8_SCALE, v_scale=FP8_SCALE)
 
 
 # -- the five configurations -------------------------------------------------
@@ -418,11 +426,19 @@ CONFIG_NAMES = {
     3: "llama3_8b_gqa_decode_b256_h32kv8_d128_p32",
     4: "llama3_70b_gqa_fp8_prefix_decode_b128_h64kv8_d128_p64",
     5: "mixed_prefill4x512_decode32_h32kv8_d128_p32",
+    # not one of the five: a longer-context chunked prefill of the same
+    # Llama-3-8B GQA shape (8 chunks of 1024 tokens onto prior contexts of
+    # 4096), for the prefill kernel's rate away from the mixed step's short
+    # contexts
+    "long_prefill": "long_prefill_8x1024_prior4096_h32kv8_d128_p32",
+    # configuration 5's batch with its KV cache stored as FP8 E4M3
+    "mixed_fp8": "mixed_prefill4x512_decode32_h32kv8_d128_p32_fp8kv",
 }
 
 
-def config(i: int, num_seqs: Optional[int] = None) -> Workload:
-    """Configuration i (1..5) at full size; seed 31000 + i.
+def config(i, num_seqs: Optional[int] = None) -> Workload:
+    """Configuration i (1..5, or "long_prefill") at full size; seed 31000 + i
+    (31006 for the long prefill).
 
     ``num_seqs`` keeps only the first sequences of the batch (same lengths,
     same shapes, a pool sized for them): a smaller case of the same kernel,
@@ -444,7 +460,14 @@ def config(i: int, num_seqs: Optional[int] = None) -> Workload:
                        num_sharers=sharers if sharers > 1 else 0)
 
 
-def _config_full(i: int) -> Workload:
+def _config_full(i) -> Workload:
+    if i == "mixed_fp8":
+        return with_fp8_kv(_config_full(5))
+    if i == "long_prefill":
+        n = 8
+        return make_mixed(CONFIG_NAMES[i], 31006, np.zeros(0, np.int32),
+                          np.full(n, 4096, np.int32), np.full(n, 1024, np.int32), 32, 8, 128, 32,
+                          max_blocks=160)
     seed = 31000 + i
     rng = np.random.Generator(np.random.PCG64(seed))
     if i == 1:
