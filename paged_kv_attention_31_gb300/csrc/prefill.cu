@@ -63,19 +63,27 @@ constexpr int kMaxRankGroups = 256;
 // starts at least 128-aligned, so at most 896 bytes of padding are needed.
 constexpr int kMaxPad = 1024 - 128;
 
+// FP8 pools: operand stages of f16 K (and V) blocks, 1 or 2; the code ring
+// of each then has 3 - that many stages (shared memory holds no more).  Two
+// operand stages let a converter work a block ahead of the MMAs (126 against
+// 149 us on the FP8 mixed step's prefill, one code stage against two).
+#ifndef PKV_PF_FP8_OPSTAGES
+#define PKV_PF_FP8_OPSTAGES 2
+#endif
+
 // Shared memory layout for head_dim D (offsets from a 1024-aligned base).
 // Rows of Q, K and V are split into D/64 halves of 64 16-bit values (128
 // bytes, one swizzle atom): a tile is [half][rows][128 B].  bf16 pools: K and
 // V stream by TMA straight into 2-stage rings of such blocks.  FP8 pools: the
-// TMA lands each key block's E4M3 codes, row-major [key][D], in a 2-stage raw
-// ring; a converter warp turns them into f16 in a 1-stage K (V) block of the
-// same swizzled layout.
+// TMA lands each key block's E4M3 codes, row-major [key][D], in a raw ring;
+// a converter warp turns them into f16 K (V) blocks of the same swizzled
+// layout.
 template <int D, bool FP8>
 struct PfLayout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStagesK = FP8 ? 1 : 2;               // K operand stages (key blocks)
-  static constexpr int kStagesV = FP8 ? 1 : 2;               // V operand stages
-  static constexpr int kRawStages = FP8 ? 2 : 0;             // FP8 code stages, each of K and V
+  static constexpr int kStagesK = FP8 ? PKV_PF_FP8_OPSTAGES : 2;  // K operand stages (key blocks)
+  static constexpr int kStagesV = FP8 ? PKV_PF_FP8_OPSTAGES : 2;  // V operand stages
+  static constexpr int kRawStages = FP8 ? 3 - PKV_PF_FP8_OPSTAGES : 0;  // code stages, K and V each
   static constexpr int kQBytes = kHalves * kM * 128;         // per tile
   static constexpr int kKVStageBytes = kHalves * kNK * 128;  // one key block of K or V
   static constexpr int kRawBytes = kNK * D;                  // one key block of FP8 codes
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lay = PfLayout<D, FP8>;
   constexpr int kHalves = Lay::kHalves, kQBytes = Lay::kQBytes;
   constexpr int kKVStageBytes = Lay::kKVStageBytes, kRawBytes = Lay::kRawBytes;
+  constexpr int kRawRing = FP8 ? Lay::kRawStages : 1;  // (the bf16 kernel has no code ring)
   constexpr int kStagesK = Lay::kStagesK, kStagesV = Lay::kStagesV;
   constexpr int kOffQ = Lay::kOffQ, kOffK = Lay::kOffK, kOffV = Lay::kOffV;
   constexpr int kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffRank = Lay::kOffRank;
@@ -472,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMA of one key block's code pages (row-major [key][D]) into raw stage
   // blk % kRawStages (whole loader warp)
   auto load_raw = [&](const CUtensorMap* map, uint8_t* raw, uint64_t* bars, int blk, int ids) {
-    const int st = blk % Lay::kRawStages;
+    const int st = blk % kRawRing;
     if (lane == 0) mbar_arrive_expect_tx(&bars[st], kRawBytes);
 #pragma unroll
     for (int i = 0; i < kNK / 16; ++i) {  // at most 8 pages per block (block_size >= 16)
@@ -484,26 +493,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the codes of one key block -> f16 in the swizzled operand layout (the
   // one a 128-byte-swizzled TMA box of 16-bit values gives); key rows from
   // zero_from on are written as zeros: slots past the sequence may hold NaN
-  // codes, and 0 * V must stay 0 in the PV product
+  // codes, and 0 * V must stay 0 in the PV product.
+  // A lane turns 16 codes (one quarter of a row half) into two 16-byte
+  // chunks.  Each group of 8 lanes (one shared-memory phase of 16-byte
+  // accesses) takes the quarters of two adjacent rows, r in one half and
+  // r + 1 in the other for D = 128 (both in the one half for D = 64), so its
+  // loads cover 128 distinct bytes of banks and its stores, whose swizzle
+  // (chunk ^ (row & 7)) differs in parity between the two rows, land in 8
+  // distinct chunk positions.  The loads of four tasks are issued before
+  // their conversions.
   auto convert_blk = [&](const uint8_t* raw, uint8_t* dst, int zero_from) {
-    constexpr int kGroups = kD / 16;  // 16-code groups per key row
-    for (int i = lane; i < kNK * kGroups; i += 32) {
-      const int r = i / kGroups, g = i - r * kGroups;
-      uint4 u = *reinterpret_cast<const uint4*>(raw + r * kD + g * 16);
-      if (r >= zero_from) u = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t f[8];
-      e4m3x4_to_f16x2(u.x, f[0], f[1]);
-      e4m3x4_to_f16x2(u.y, f[2], f[3]);
-      e4m3x4_to_f16x2(u.z, f[4], f[5]);
-      e4m3x4_to_f16x2(u.w, f[6], f[7]);
-      // values 16g .. 16g + 15: half 16g / 64, 16-byte chunks c and c + 1
-      const int dh = (16 * g) / 64, c = ((16 * g) % 64) / 8;
-      uint8_t* row = dst + dh * (kNK * 128) + r * 128;
-      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<uint4*>(row + (((c + 1) ^ (r & 7)) << 4)) =
-          make_uint4(f[4], f[5], f[6], f[7]);
+    constexpr int kTasks = kNK * kHalves * 4;  // 16-code tasks per block
+    constexpr int kBatch = 4;                  // tasks in flight per lane
+    static_assert(kTasks % (32 * kBatch) == 0, "whole batches");
+    for (int i0 = 0; i0 < kTasks; i0 += 32 * kBatch) {
+      uint4 u[kBatch];
+      int row[kBatch], hf[kBatch], qt[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * 32 + lane;
+        const int g = i >> 3, w = i & 7;       // phase group, lane in it
+        const int pr = w >> 2;                 // which row of the pair
+        qt[b] = w & 3;                         // quarter of the half row
+        if constexpr (kHalves == 2) {          // groups alternate the half pairing
+          row[b] = 2 * (g >> 1) + pr;
+          hf[b] = pr ^ (g & 1);
+        } else {
+          row[b] = 2 * g + pr;
+          hf[b] = 0;
+        }
+        u[b] = *reinterpret_cast<const uint4*>(raw + row[b] * kD + hf[b] * 64 + qt[b] * 16);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const uint4 v = row[b] >= zero_from ? make_uint4(0u, 0u, 0u, 0u) : u[b];
+        uint32_t f[8];
+        e4m3x4_to_f16x2(v.x, f[0], f[1]);
+        e4m3x4_to_f16x2(v.y, f[2], f[3]);
+        e4m3x4_to_f16x2(v.z, f[4], f[5]);
+        e4m3x4_to_f16x2(v.w, f[6], f[7]);
+        uint8_t* const d = dst + hf[b] * (kNK * 128) + row[b] * 128;
+        const int c = 2 * qt[b], x = row[b] & 7;
+        *reinterpret_cast<uint4*>(d + ((c ^ x) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<uint4*>(d + (((c + 1) ^ x) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+      }
     }
   };
+
   // a converter warp keeps kRawStages code blocks in flight; block b is
   // converted into operand stage b % stages once `freed` says the MMAs that
   // read its previous block are done, and `ready` then signals the MMA warp.
@@ -511,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // copies in flight have landed.
   auto run_converter = [&](const CUtensorMap* map, uint8_t* raw, uint64_t* raw_full,
                            uint8_t* ops, uint64_t* ready, uint64_t* freed, int stages) {
-    constexpr int R = Lay::kRawStages;
+    constexpr int R = kRawRing;
     constexpr int kLead = 3;  // page ids are read kLead blocks ahead
     int ids[kLead];
 #pragma unroll
