@@ -63,6 +63,12 @@ constexpr int kMaxRankGroups = 256;
 // starts at least 128-aligned, so at most 896 bytes of padding are needed.
 constexpr int kMaxPad = 1024 - 128;
 
+// 1: the softmax skips its max pass where the block's P sum shows that the
+// lagged running max need not move (0: a max pass on every block).
+#ifndef PKV_PF_SKIP_MAX
+#define PKV_PF_SKIP_MAX 1
+#endif
+
 // FP8 pools: operand stages of f16 K (and V) blocks, 1 or 2; the code ring
 // of each then has 3 - that many stages (shared memory holds no more).  Two
 // operand stages let a converter work a block ahead of the MMAs (126 against
@@ -782,9 +788,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kbase = j * kNK;
       const bool diag = kbase + kNK - 1 > minpos;   // causal mask inside this block
-      // The softmax is issue-bound: per score it spends half a 3-input max
-      // (pass 1), half a packed FMA, one ex2, half a packed add and half a
-      // bf16x2 conversion (pass 2); masks cost extra only in diagonal blocks.
+      // The softmax is issue-bound: per score it spends half a packed FMA,
+      // one ex2, half a packed add and half a 16-bit-pair conversion (the P
+      // pass), and half a 3-input max in the blocks that need a max pass;
+      // masks cost extra only in diagonal blocks.
       // tcgen05.ld / st are warp-collective: every lane runs them, whatever
       // its row (rows past the chunk compute unused values).
       // The block's 128 scores in one tcgen05.ld, kept in registers for both
@@ -795,49 +802,68 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kNK; ++i) sv[i] = (kbase + i <= pos) ? sv[i] : -INFINITY;
       }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Block max and lagged running max: the max moves only when the block
+      // max exceeds it by more than 8 (log2 domain), so P <= 2^8.  The max
+      // pass runs where a row has no running max yet (its first block);
+      // elsewhere P is computed with the running max first and the block's
+      // P sum decides: a sum above 2^15 = 128 x 2^8 means some P exceeds 2^8
+      // (the running max must move), and the block is redone after a max
+      // pass.  Otherwise every P <= 2^15 fits the 16-bit operand type and the
+      // max pass is skipped.  Rows past the chunk take no part in either test.
+      float alpha = 1.f, blk_sum = 0.f;
+      bool do_max = PKV_PF_SKIP_MAX == 0 ||
+                    __any_sync(0xffffffffu, row_valid && m_used == -INFINITY);
+#pragma unroll 1
+      for (;;) {
+        if (do_max) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < kNK; i += 8) {
-        m4[0] = fmax3(m4[0], sv[i], sv[i + 1]);
-        m4[1] = fmax3(m4[1], sv[i + 2], sv[i + 3]);
-        m4[2] = fmax3(m4[2], sv[i + 4], sv[i + 5]);
-        m4[3] = fmax3(m4[3], sv[i + 6], sv[i + 7]);
-      }
-      const float mx = row_valid ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qm
-                                 : -INFINITY;  // log2 domain (qm > 0)
-      // lagged running max: move it only when the block max exceeds it by > 8
-      float alpha = 1.f;
-      if (mx > m_used + 8.f) {
-        alpha = fast_exp2(m_used - mx);  // 0 when m_used = -inf
-        m_used = mx;
-        l_sum *= alpha;
-      }
-      // P = 2^(s * qm - m) as bf16 pairs over the first half of S's columns
-      // (chunk c's pairs land in columns c/2 .. c/2 + 15; S is already in
-      // registers); masked scores are -inf and give 0
-      const float negm = m_used != -INFINITY ? -m_used : 0.f;
-      const float2 qm2 = make_float2(qm, qm), nm2 = make_float2(negm, negm);
-      float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < kNK; c += 32) {
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x2 = __ffma2_rn(make_float2(sv[c + i], sv[c + i + 1]), qm2, nm2);
-          const float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
-          acc2[(i >> 1) & 1] = __fadd2_rn(acc2[(i >> 1) & 1], e2);
-          if constexpr (FP8) {  // the PV product's operands are f16
-            const __half2 ph = __floats2half2_rn(e2.x, e2.y);
-            pw[i / 2] = *reinterpret_cast<const uint32_t*>(&ph);
-          } else {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
-            pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          for (int i = 0; i < kNK; i += 8) {
+            m4[0] = fmax3(m4[0], sv[i], sv[i + 1]);
+            m4[1] = fmax3(m4[1], sv[i + 2], sv[i + 3]);
+            m4[2] = fmax3(m4[2], sv[i + 4], sv[i + 5]);
+            m4[3] = fmax3(m4[3], sv[i + 6], sv[i + 7]);
+          }
+          const float mx = row_valid ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qm
+                                     : -INFINITY;  // log2 domain (qm > 0)
+          if (mx > m_used + 8.f) {
+            const float a = fast_exp2(m_used - mx);  // 0 when m_used = -inf
+            alpha *= a;
+            m_used = mx;
+            l_sum *= a;
           }
         }
-        tmem_st16_async(tmem + lane_base + colS + c / 2, pw);
+        // P = 2^(s * qm - m) as 16-bit pairs over the first half of S's
+        // columns (chunk c's pairs land in columns c/2 .. c/2 + 15; S is
+        // already in registers); masked scores are -inf and give 0
+        const float negm = m_used != -INFINITY ? -m_used : 0.f;
+        const float2 qm2 = make_float2(qm, qm), nm2 = make_float2(negm, negm);
+        float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < kNK; c += 32) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x2 = __ffma2_rn(make_float2(sv[c + i], sv[c + i + 1]), qm2, nm2);
+            const float2 e2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+            acc2[(i >> 1) & 1] = __fadd2_rn(acc2[(i >> 1) & 1], e2);
+            if constexpr (FP8) {  // the PV product's operands are f16
+              const __half2 ph = __floats2half2_rn(e2.x, e2.y);
+              pw[i / 2] = *reinterpret_cast<const uint32_t*>(&ph);
+            } else {
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(e2.x, e2.y);
+              pw[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+            }
+          }
+          tmem_st16_async(tmem + lane_base + colS + c / 2, pw);
+        }
+        const float2 a2 = __fadd2_rn(acc2[0], acc2[1]);
+        blk_sum = a2.x + a2.y;
+        if (do_max || !__any_sync(0xffffffffu, row_valid && blk_sum > 32768.f)) break;
+        do_max = true;   // (rare) redo the block after the max pass
+        tmem_wait_st();  // the stores above land before the ones that replace them
       }
-      const float2 a = __fadd2_rn(acc2[0], acc2[1]);
-      l_sum += a.x + a.y;
+      l_sum += blk_sum;
 
       // O rescale (rare: the running max moves by > 2^8 only early in a row).
       // PV_{j-1} is complete: the commit behind "S_j ready" covers it.
