@@ -721,6 +721,20 @@ def _measure(w, a, dev, peaks, peak_kind, world):
     return line
 
 
+def _prefill_l2_note(w, dev):
+    """How the prefill-only timing relates to the L2: its pages and q."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 129 * 2 ** 20
+    per_tok = w.num_kv_heads * 2 * w.head_dim * w.elem_bytes
+    working = (int(np.sum(w.prefill_context_lens, dtype=np.int64)) * per_tok +
+               w.num_prefill_tokens * w.num_q_heads * w.head_dim * 2 * 2)
+    return (f"no flush: each call reads {working / 2 ** 20:.0f} MB of pages and q and writes its "
+            f"output, more than the {l2 >> 20} MB L2 (the call is bound by the tensor cores)"
+            if working > l2 else
+            f"no flush: the {working / 2 ** 20:.0f} MB working set fits in the {l2 >> 20} MB L2 "
+            f"(the call is bound by the tensor cores)")
+
+
 def _measure_prefill_only(w, a, dev, peaks, peak_kind, world):
     """Chunked prefill alone (its rows appended once, untimed): the prefill
     call timed back to back over a.steps calls, then with events around each
@@ -782,7 +796,8 @@ def _measure_prefill_only(w, a, dev, peaks, peak_kind, world):
                                           w.prefill_context_lens - w.prefill_chunk_lens],
                    "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size,
-                   "kv_dtype": w.kv_dtype, "step_calls": "pkv_paged_prefill"},
+                   "kv_dtype": w.kv_dtype, "step_calls": "pkv_paged_prefill",
+                   "l2": _prefill_l2_note(w, dev)},
         "tokens_per_s": world * w.num_prefill_tokens / (chain_ms * 1e-3),
         "roofline": {"bound": "tensor", "achieved": flops / (call_ms * 1e-3) / 1e12,
                      "peak": tpeak, "unit": "TFLOP/s",

@@ -405,7 +405,8 @@ PKV_API pkv_status pkv_cache_block_tables(const pkv_cache *cache, const int64_t 
 /* Static string for a status code (never NULL). */
 PKV_API const char *pkv_status_string(int32_t status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  101: pkv_paged_prefill accepts
+ * FP8 E4M3 pools. */
 PKV_API int32_t pkv_version(void);
 
 #ifdef __cplusplus

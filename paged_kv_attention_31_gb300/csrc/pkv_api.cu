@@ -144,7 +144,7 @@ __global__ void take_error_kernel(int32_t* err, int32_t* taken) { *taken = atomi
 
 extern "C" {
 
-int32_t pkv_version(void) { return 100; }
+int32_t pkv_version(void) { return 101; }
 
 const char* pkv_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 

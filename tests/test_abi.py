@@ -37,7 +37,7 @@ def test_header_declares_the_entry_points():
 def test_every_declared_symbol_is_exported(lib):
     for name in _declared():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.pkv_version() == 100
+    assert lib.pkv_version() == 101
 
 
 def test_internal_symbols_hidden(lib):

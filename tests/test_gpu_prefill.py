@@ -243,13 +243,15 @@ def test_fp8_never_written_slots_past_the_end_do_not_leak():
 
 
 @pytest.mark.parametrize("mult,scale_div", [(2.0 ** 16, 2.0 ** 16), (2.0 ** -20, 2.0 ** -20),
-                                            (300.0, 1.0)])
-def test_fp8_pool_q_far_from_unit_scale(mult, scale_div):
+                                            (300.0, 1.0), (1e-5, 1.0)])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_q_far_from_unit_scale(mult, scale_div, kv_dtype):
     # q rows far outside f16's range (or deep in its subnormals), the softmax
-    # scale divided by the same power of two: the per-row power-of-two
-    # scaling before the f16 conversion keeps the scores exact
-    w = W.make_mixed("prefill_fp8_qrange", 7321, [20], [0, 90], [70, 150], 32, 8, 128, 32,
-                     kv_dtype="fp8_e4m3")
+    # scale divided by the same power of two: over an FP8 pool the per-row
+    # power-of-two scaling before the f16 conversion keeps the scores exact;
+    # over a bf16 pool q is used as it is
+    w = W.make_mixed(f"prefill_qrange_{kv_dtype}", 7321, [20], [0, 90], [70, 150], 32, 8, 128,
+                     32, kv_dtype=kv_dtype)
     d = device_step_inputs(w)
     kp, vp = device_pools(w)
     pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale)
@@ -267,7 +269,8 @@ def test_fp8_pool_q_far_from_unit_scale(mult, scale_div):
         for h in (0, w.num_kv_heads - 1):
             kv = (W.bf16_bits(kn[:, h, :]), W.bf16_bits(vn[:, h, :]))
             want = _oracle_prefill_rows_q(w, s, h, kv, q_host, scale)
-            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, True, f"s={s} h={h}")
+            assert_close(out[cu[s]:cu[s + 1], h * G:(h + 1) * G], want, kv_dtype != "bf16",
+                         f"s={s} h={h}")
 
 
 def _oracle_prefill_rows_q(w, s, h, kv, q_host, scale):
