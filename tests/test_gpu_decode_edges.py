@@ -120,3 +120,25 @@ def test_never_written_slots_fused_step(kv_dtype):
     assert pkv.get_device_error() == 0
     assert torch.isfinite(out.float()).all()
     _check(w, out)
+
+
+@pytest.mark.parametrize("G,D,P", [(8, 128, 32), (4, 128, 16), (2, 128, 64)])
+def test_q_range_with_per_head_fp8_scales(G, D, P):
+    # the per-head q scaling of the tensor-core decode combined with per-kv-head
+    # K / V scales (both multiply the same scores), q at 2^16 with the softmax
+    # scale divided by 2^16
+    hkv = 4
+    w = W.with_head_scales(W.make_decode(f"qrange_heads_G{G}_D{D}_P{P}", 4700 + G + P, LENS,
+                                         hkv * G, hkv, D, P, kv_dtype="fp8_e4m3"))
+    q_host = (w.q_decode().float() * 2.0 ** 16).to(torch.bfloat16)
+    scale = w.scale / 2.0 ** 16
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    ks, vs = w.scale_tensors("cuda")
+    pkv.kv_append(d["k_new"], d["v_new"], d["slots"], kp, vp, w.k_scale, w.v_scale,
+                  k_scales=ks, v_scales=vs)
+    out = pkv.paged_attention(q_host.to("cuda"), kp, vp, d["block_tables"], d["context_lens"],
+                              w.max_context_len, scale, k_scale=w.k_scale, v_scale=w.v_scale,
+                              partition_tokens=256, k_scales=ks, v_scales=vs)
+    assert pkv.get_device_error() == 0
+    _check(w, out, q_host=q_host, scale=scale)
