@@ -94,10 +94,11 @@ struct PfLayout {
   static constexpr int kKVStageBytes = kHalves * kNK * 128;  // one key block of K or V
   static constexpr int kRawBytes = kNK * D;                  // one key block of FP8 codes
   // barriers: q, k[SK], kfree[SK], v[SV], vfree[SV], s[tiles], p[tiles],
-  // o[tiles], drain (the MMA warp's last commit after an abort); FP8 also
-  // qc (Q converted), kraw[R], vraw[R] (code blocks landed)
+  // o[tiles], drain (the MMA thread's last commit after an abort), vz (the
+  // last V block's rows past the sequence zeroed); FP8 also qc (Q
+  // converted), kraw[R], vraw[R] (code blocks landed)
   static constexpr int kNumBars =
-      1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles + 1 + (FP8 ? 1 + 2 * kRawStages : 0);
+      1 + 2 * kStagesK + 2 * kStagesV + 3 * kTiles + 2 + (FP8 ? 1 + 2 * kRawStages : 0);
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTiles * kQBytes;
   static constexpr int kOffV = kOffK + kStagesK * kKVStageBytes;
@@ -372,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_p = bar_s + kTiles;               // [kTiles] P_t written (4 warps)
   uint64_t* bar_o = bar_p + kTiles;               // [kTiles] last PV of tile t done (one phase)
   uint64_t* bar_drain = bar_o + kTiles;           // every issued MMA done (after an abort)
+  uint64_t* bar_vz = bar_drain + 1;               // bf16: last V block's tail rows zeroed
   // FP8 only: Q converted to f16 (8 softmax warps), code blocks landed
-  uint64_t* bar_qc = bar_drain + 1;
+  uint64_t* bar_qc = bar_vz + 1;
   uint64_t* bar_kraw = bar_qc + 1;                // [kRawStages]
   uint64_t* bar_vraw = bar_kraw + Lay::kRawStages;  // [kRawStages]
   uint8_t* sRawK = smem + Lay::kOffRawK;
@@ -408,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_o[t], 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_vz, 1);
     if constexpr (FP8) {
       mbar_init(bar_qc, 8);
       for (int i = 0; i < Lay::kRawStages; ++i) {
@@ -456,11 +459,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // a loader streams blocks 0 .. nblk-1 into its ring; block b reuses the
   // stage of block b - stages once `freed` says the MMAs reading it are done.
+  // With `tail_bar` (the V ring) and a last block that reaches past the
+  // sequence, the loader waits for that block to land, zeroes its rows from
+  // the sequence end on (never-written slots may hold NaN, and 0 * V must
+  // stay 0 in the PV product) and then arrives on `tail_bar`, which the MMA
+  // thread waits instead of the block's own barrier.
   // If a wait gives up it stops issuing; either way it returns only after
   // the copies it issued into the ring have landed (on the normal path the
-  // MMA warp has already seen them all, so this returns at once).
+  // MMA thread has already seen them all, so this returns at once).
   auto run_loader = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* freed,
-                        int stages) {
+                        int stages, uint64_t* tail_bar) {
     constexpr int kLead = 3;  // page ids are read kLead blocks ahead
     int ids[kLead];
 #pragma unroll
@@ -476,6 +484,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k + 1 < kLead; ++k) ids[k] = ids[k + 1];
       ids[kLead - 1] = fetch_ids(b + kLead);
+      if (tail_bar != nullptr && b == nblk - 1 && b * kNK + kNK > L) {
+        if (!warp_wait_bounded(&full[b % stages], uint32_t(b / stages) & 1, p.err, abort_flag))
+          break;
+        uint8_t* const st = ring + (b % stages) * kKVStageBytes;
+        const int first = max(0, L - b * kNK);
+        for (int i = lane; i < (kNK - first) * 8 * kHalves; i += 32) {
+          const int r = first + i / (8 * kHalves), dh = (i / 8) % kHalves, chunk = i % 8;
+          *reinterpret_cast<uint4*>(st + dh * (kNK * 128) + r * 128 + chunk * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // the PV MMAs (async proxy) read the block next
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tail_bar);
+      }
     }
     if (lane == 0)
       for (int b = max(0, issued - stages); b < issued; ++b)
@@ -599,121 +621,113 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (FP8)
       run_converter(&tm_k, sRawK, bar_kraw, sK, bar_k, bar_kfree, kStagesK);
     else
-      run_loader(&tm_k, sK, bar_k, bar_kfree, kStagesK);
+      run_loader(&tm_k, sK, bar_k, bar_kfree, kStagesK, nullptr);
     if (lane == 0) mbar_drain_wait(bar_q, 0, p.err);  // Q landed (normally seen long ago)
     __syncwarp();
   } else if (warp == kVLoadWarp) {
     if constexpr (FP8)
       run_converter(&tm_v, sRawV, bar_vraw, sV, bar_v, bar_vfree, kStagesV);
     else
-      run_loader(&tm_v, sV, bar_v, bar_vfree, kStagesV);
+      run_loader(&tm_v, sV, bar_v, bar_vfree, kStagesV, bar_vz);
   } else if (warp == kMmaWarp) {
-    constexpr uint32_t kIdescS = idesc_f16_kind(kM, kNK, false, FP8);
-    constexpr uint32_t kIdescO = idesc_f16_kind(kM, kD, true, FP8);
-    auto issue_s = [&](int t, int blk) {  // lane 0: S_t of block blk
-      const uint32_t qa = smem_u32(sQ + t * kQBytes);
-      const uint32_t ka = smem_u32(sK + (blk % kStagesK) * kKVStageBytes);
+    // One thread issues every MMA and waits on every barrier of this loop.  A
+    // tcgen05.mma issue proceeds at about the tensor core's own pace (only a
+    // few products queue ahead), so the thread's path from one tile's last
+    // product to the other tile's first must stay short, or the tensor core
+    // idles: no warp-wide votes or syncs inside the loop.
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_f16_kind(kM, kNK, false, FP8);
+      constexpr uint32_t kIdescO = idesc_f16_kind(kM, kD, true, FP8);
+      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+      auto issue_s = [&](int t, int blk) {  // S_t of block blk
+        const uint32_t qa = q_base + t * kQBytes;
+        const uint32_t ka = k_base + (blk % kStagesK) * kKVStageBytes;
 #pragma unroll
-      for (int ks = 0; ks < kD / 16; ++ks) {
-        const int dh = ks >> 2, w = ks & 3;
-        const uint64_t ad = sw128_desc(qa + dh * (kM * 128) + w * 32, 16, 1024);
-        const uint64_t bd = sw128_desc(ka + dh * (kNK * 128) + w * 32, 16, 1024);
-        mma_bf16(tmem + kColS + t * kNK, ad, bd, kIdescS, ks > 0);
-      }
-      mma_commit(&bar_s[t]);
-    };
-    auto issue_pv = [&](int t, int blk, bool last) {  // lane 0: O_t += P_t V_blk
-      const uint32_t va = smem_u32(sV + (blk % kStagesV) * kKVStageBytes);
-#pragma unroll
-      for (int ks = 0; ks < kNK / 16; ++ks) {
-        const uint64_t bd = sw128_desc(va + ks * 2048, kNK * 128, 1024);
-        mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8, bd, kIdescO,
-                    (blk > 0 || ks > 0) ? 1u : 0u);
-      }
-      if (last) mma_commit(&bar_o[t]);
-    };
-    auto wait_k = [&](int b) {
-      return warp_wait_bounded(&bar_k[b % kStagesK], uint32_t(b / kStagesK) & 1, p.err,
-                               abort_flag);
-    };
-
-    // `alive` turns false when a wait gives up: no further MMA is issued.
-    // FP8: Q is read once the softmax warps have converted it to f16.
-    bool alive = warp_wait_bounded(FP8 ? bar_qc : bar_q, 0, p.err, abort_flag);
-    if (alive && nblk > 0) {
-      alive = wait_k(0);
-      if (alive && lane == 0) {
-        tc_fence_after();
-        if (nb0 > 0) issue_s(0, 0);
-        if (nb1 > 0) issue_s(1, 0);
-        mma_commit(&bar_kfree[0]);
-      }
-      __syncwarp();
-    }
-    for (int j = 0; alive && j < nblk; ++j) {
-      const int sv = j % kStagesV;
-      // V_j landed; rows past the sequence end may hold never-written slots:
-      // zero them so that 0 * V stays 0 in the PV product
-      if (!warp_wait_bounded(&bar_v[sv], uint32_t(j / kStagesV) & 1, p.err, abort_flag)) {
-        alive = false;
-        break;
-      }
-      if (!FP8 && j * kNK + kNK > L) {  // (FP8: the converter wrote those rows as zeros)
-        const int first = max(0, L - j * kNK);
-        for (int i = lane; i < (kNK - first) * 8 * kHalves; i += 32) {
-          const int r = first + i / (8 * kHalves), dh = (i / 8) % kHalves, chunk = i % 8;
-          *reinterpret_cast<uint4*>(sV + sv * kKVStageBytes + dh * (kNK * 128) + r * 128 +
-                                    chunk * 16) = make_uint4(0, 0, 0, 0);
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const int dh = ks >> 2, w = ks & 3;
+          const uint64_t ad = sw128_desc(qa + dh * (kM * 128) + w * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(ka + dh * (kNK * 128) + w * 32, 16, 1024);
+          mma_bf16(tmem + kColS + t * kNK, ad, bd, kIdescS, ks > 0);
         }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      // per tile: O_t += P_t V_j once the softmax warps have written P_t, then
-      // S_t of block j + 1 into the same TMEM columns (the tensor core runs
-      // MMAs in issue order, so the PV has read P before S overwrites it)
-      bool k_ready = false;
+        mma_commit(&bar_s[t]);
+      };
+      auto issue_pv = [&](int t, int blk, bool last) {  // O_t += P_t V_blk
+        const uint32_t va = v_base + (blk % kStagesV) * kKVStageBytes;
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t) {
-        const int nbt = t == 0 ? nb0 : nb1;
-        if (j >= nbt) continue;
-        if (!warp_wait_bounded(&bar_p[t], uint32_t(j) & 1, p.err, abort_flag)) {
+        for (int ks = 0; ks < kNK / 16; ++ks) {
+          const uint64_t bd = sw128_desc(va + ks * 2048, kNK * 128, 1024);
+          mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8, bd, kIdescO,
+                      (blk > 0 || ks > 0) ? 1u : 0u);
+        }
+        if (last) mma_commit(&bar_o[t]);
+      };
+      auto wait_k = [&](int b) {
+        return mbar_wait_bounded(&bar_k[b % kStagesK], uint32_t(b / kStagesK) & 1, p.err,
+                                 abort_flag);
+      };
+      // bf16: a last V block reaching past the sequence is handed over by
+      // the V loader once it has zeroed the rows there (FP8: the converter
+      // writes those rows as zeros)
+      const bool vtail = !FP8 && nblk * kNK > L;
+
+      // `alive` turns false when a wait gives up: no further MMA is issued.
+      // FP8: Q is read once the softmax warps have converted it to f16.
+      bool alive = mbar_wait_bounded(FP8 ? bar_qc : bar_q, 0, p.err, abort_flag);
+      if (alive && nblk > 0) {
+        alive = wait_k(0);
+        if (alive) {
+          tc_fence_after();
+          if (nb0 > 0) issue_s(0, 0);
+          if (nb1 > 0) issue_s(1, 0);
+          mma_commit(&bar_kfree[0]);
+        }
+      }
+      for (int j = 0; alive && j < nblk; ++j) {
+        const int sv = j % kStagesV;
+        const bool z = vtail && j == nblk - 1;
+        if (!mbar_wait_bounded(z ? bar_vz : &bar_v[sv], z ? 0u : uint32_t(j / kStagesV) & 1,
+                               p.err, abort_flag)) {
           alive = false;
           break;
         }
-        if (lane == 0) {
+        // per tile: O_t += P_t V_j once the softmax warps have written P_t,
+        // then S_t of block j + 1 into the same TMEM columns (the tensor core
+        // runs MMAs in issue order, so the PV has read P before S overwrites it)
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          const int nbt = t == 0 ? nb0 : nb1;
+          if (j >= nbt) continue;
+          if (!mbar_wait_bounded(&bar_p[t], uint32_t(j) & 1, p.err, abort_flag)) {
+            alive = false;
+            break;
+          }
           tc_fence_after();
           issue_pv(t, j, j == nbt - 1);
-        }
-        __syncwarp();
-        if (j + 1 < nbt) {
-          if (!k_ready) {
-            if (!wait_k(j + 1)) {
-              alive = false;
-              break;
+          if (j + 1 < nbt) {
+            if (!k_ready) {
+              if (!wait_k(j + 1)) {
+                alive = false;
+                break;
+              }
+              k_ready = true;
             }
-            k_ready = true;
+            issue_s(t, j + 1);
           }
-          if (lane == 0) issue_s(t, j + 1);
-          __syncwarp();
         }
-      }
-      if (!alive) break;
-      // stage release: V_j after both tiles' PV, K_{j+1} after both tiles' S
-      if (lane == 0) {
+        if (!alive) break;
+        // stage release: V_j after both tiles' PV, K_{j+1} after both tiles' S
         mma_commit(&bar_vfree[sv]);
         if (j + 1 < nblk) mma_commit(&bar_kfree[(j + 1) % kStagesK]);
       }
-      __syncwarp();
-    }
-    if (!alive) {
-      // every MMA this thread issued completes before TMEM is released (a
-      // commit arrives once all of the thread's earlier MMAs are done)
-      if (lane == 0) {
+      if (!alive) {
+        // every MMA this thread issued completes before TMEM is released (a
+        // commit arrives once all of the thread's earlier MMAs are done)
         mma_commit(bar_drain);
         mbar_drain_wait(bar_drain, 0, p.err);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else if (warp < kMmaWarp) {
     // ================================ softmax ====================================
     const int t = warp >> 2;                        // tile of this warpgroup
