@@ -639,25 +639,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = idesc_f16_kind(kM, kNK, false, FP8);
       constexpr uint32_t kIdescO = idesc_f16_kind(kM, kD, true, FP8);
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-      auto issue_s = [&](int t, int blk) {  // S_t of block blk
-        const uint32_t qa = q_base + t * kQBytes;
-        const uint32_t ka = k_base + (blk % kStagesK) * kKVStageBytes;
+      // shared-memory descriptors of every operand step, made once: the
+      // issuing thread's path per MMA is then the instruction itself
+      static_assert(kStagesK == 2 && kStagesV == 2, "two operand stages");
+      uint64_t dq[kTiles][kD / 16], dk[2][kD / 16], dv[2][kNK / 16];
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const int dh = ks >> 2, w = ks & 3;
-          const uint64_t ad = sw128_desc(qa + dh * (kM * 128) + w * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(ka + dh * (kNK * 128) + w * 32, 16, 1024);
-          mma_bf16(tmem + kColS + t * kNK, ad, bd, kIdescS, ks > 0);
-        }
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        const int dh = ks >> 2, w = ks & 3;
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t)
+          dq[t][ks] = sw128_desc(q_base + t * kQBytes + dh * (kM * 128) + w * 32, 16, 1024);
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          dk[st][ks] =
+              sw128_desc(k_base + st * kKVStageBytes + dh * (kNK * 128) + w * 32, 16, 1024);
+      }
+#pragma unroll
+      for (int ks = 0; ks < kNK / 16; ++ks)
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          dv[st][ks] = sw128_desc(v_base + st * kKVStageBytes + ks * 2048, kNK * 128, 1024);
+      auto issue_s = [&](int t, int blk) {  // S_t of block blk
+        const bool st = (blk & 1) != 0;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks)
+          mma_bf16(tmem + kColS + t * kNK, dq[t][ks], st ? dk[1][ks] : dk[0][ks], kIdescS,
+                   ks > 0);
         mma_commit(&bar_s[t]);
       };
       auto issue_pv = [&](int t, int blk, bool last) {  // O_t += P_t V_blk
-        const uint32_t va = v_base + (blk % kStagesV) * kKVStageBytes;
+        const bool st = (blk & 1) != 0;
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks) {
-          const uint64_t bd = sw128_desc(va + ks * 2048, kNK * 128, 1024);
-          mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8, bd, kIdescO,
-                      (blk > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8,
+                      st ? dv[1][ks] : dv[0][ks], kIdescO, (blk > 0 || ks > 0) ? 1u : 0u);
         }
         if (last) mma_commit(&bar_o[t]);
       };
