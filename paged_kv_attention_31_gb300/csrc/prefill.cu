@@ -817,10 +817,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kbase = j * kNK;
       const bool diag = kbase + kNK - 1 > minpos;   // causal mask inside this block
-      // The softmax is issue-bound: per score it spends half a packed FMA,
-      // one ex2, half a packed add and half a 16-bit-pair conversion (the P
-      // pass), and half a 3-input max in the blocks that need a max pass;
-      // masks cost extra only in diagonal blocks.
+      // Per score the softmax spends half a packed FMA, one ex2, half a
+      // packed add and half a 16-bit-pair conversion (the P pass), and half
+      // a 3-input max in the blocks that need a max pass; masks cost extra
+      // only in diagonal blocks.  One warp's pass is a chain of dependent
+      // steps per pair of scores and takes about 2.7 times its ex2 issue time
+      // (ex2.approx.f32: 4 cycles per warp instruction per sub-partition).
       // tcgen05.ld / st are warp-collective: every lane runs them, whatever
       // its row (rows past the chunk compute unused values).
       // The block's 128 scores in one tcgen05.ld, kept in registers for both
