@@ -16,21 +16,25 @@
 //               pages (warp 10) into 2-stage rings of 128-key blocks shared
 //               by both tiles; page ids from the block table, read a few
 //               blocks ahead; pages past the sequence use an out-of-range
-//               coordinate so TMA fills zeros.
-//   warp 8      every tcgen05.mma (one elected lane):
+//               coordinate so TMA fills zeros; the V loader zeroes the last
+//               block's rows past the sequence end before handing it over.
+//   warp 8      lane 0 alone issues every tcgen05.mma and waits on every
+//               barrier of its loop, with descriptors made once per CTA:
 //                 S_t = Q_t K_j^T  (M=128, N=128, K=128; A, B in shared memory)
 //                 O_t += P_t V_j   (M=128, N=128, K=128; A = P in TMEM, B = V)
 //   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: one thread
-//   warps 4-7   per row (TMEM lane).  A first pass over S (tcgen05.ld) takes
-//               the block max with the causal mask; the running max moves
-//               only when it grows by more than 2^8 (O is then rescaled in
-//               TMEM; the final normalisation uses the same max, so the
-//               result is exact); a second pass writes P = 2^(s - m) as bf16
-//               pairs over the first half of S's own TMEM columns.
+//   warps 4-7   per row (TMEM lane).  One tcgen05.ld brings a block's 128
+//               scores into registers (causal mask on diagonal blocks); the
+//               running max is lagged: it moves only when it grows by more
+//               than 2^8 (O is then rescaled in TMEM; the final
+//               normalisation uses the same max, so the result is exact),
+//               and the block-max pass runs only where that can happen; P =
+//               2^(s - m) goes as bf16 pairs over the first half of S's own
+//               TMEM columns.
 // TMEM (512 columns): S_t at 128 t, O_t at 256 + 128 t.  P never leaves
 // TMEM: the PV product reads its A operand there, so shared memory holds
 // only Q, K and V and feeds one operand per PV MMA.  Per tile the chain is
-// S_j -> softmax_j -> (PV_j, S_{j+1}); the MMA warp alternates the tiles, so
+// S_j -> softmax_j -> (PV_j, S_{j+1}); the MMA issuer alternates the tiles, so
 // while one tile's softmax runs the tensor core works on the other tile.
 // Every hand-off is an mbarrier: tcgen05.commit signals "S ready", "last PV
 // done" and "K / V stage free"; the softmax warps signal "P ready".  The
