@@ -75,8 +75,8 @@ constexpr int kMaxPad = 1024 - 128;
 
 // FP8 pools: operand stages of f16 K (and V) blocks, 1 or 2; the code ring
 // of each then has 3 - that many stages (shared memory holds no more).  Two
-// operand stages let a converter work a block ahead of the MMAs (126 against
-// 149 us on the FP8 mixed step's prefill, one code stage against two).
+// operand stages let a converter work a block ahead of the MMAs (87 against
+// 105 us on the FP8 mixed step's prefill, one code stage against two).
 #ifndef PKV_PF_FP8_OPSTAGES
 #define PKV_PF_FP8_OPSTAGES 2
 #endif
@@ -645,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
       // shared-memory descriptors of every operand step, made once: the
       // issuing thread's path per MMA is then the instruction itself
-      static_assert(kStagesK == 2 && kStagesV == 2, "two operand stages");
-      uint64_t dq[kTiles][kD / 16], dk[2][kD / 16], dv[2][kNK / 16];
+      static_assert(kStagesK <= 2 && kStagesV <= 2, "one or two operand stages");
+      uint64_t dq[kTiles][kD / 16], dk[kStagesK][kD / 16], dv[kStagesV][kNK / 16];
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
         const int dh = ks >> 2, w = ks & 3;
@@ -654,29 +654,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kTiles; ++t)
           dq[t][ks] = sw128_desc(q_base + t * kQBytes + dh * (kM * 128) + w * 32, 16, 1024);
 #pragma unroll
-        for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < kStagesK; ++st)
           dk[st][ks] =
               sw128_desc(k_base + st * kKVStageBytes + dh * (kNK * 128) + w * 32, 16, 1024);
       }
 #pragma unroll
       for (int ks = 0; ks < kNK / 16; ++ks)
 #pragma unroll
-        for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < kStagesV; ++st)
           dv[st][ks] = sw128_desc(v_base + st * kKVStageBytes + ks * 2048, kNK * 128, 1024);
       auto issue_s = [&](int t, int blk) {  // S_t of block blk
-        const bool st = (blk & 1) != 0;
+        const bool st = kStagesK == 2 && (blk & 1) != 0;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks)
-          mma_bf16(tmem + kColS + t * kNK, dq[t][ks], st ? dk[1][ks] : dk[0][ks], kIdescS,
-                   ks > 0);
+          mma_bf16(tmem + kColS + t * kNK, dq[t][ks], st ? dk[kStagesK - 1][ks] : dk[0][ks],
+                   kIdescS, ks > 0);
         mma_commit(&bar_s[t]);
       };
       auto issue_pv = [&](int t, int blk, bool last) {  // O_t += P_t V_blk
-        const bool st = (blk & 1) != 0;
+        const bool st = kStagesV == 2 && (blk & 1) != 0;
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks) {
           mma_bf16_ts(tmem + kColO + t * kD, tmem + kColS + t * kNK + ks * 8,
-                      st ? dv[1][ks] : dv[0][ks], kIdescO, (blk > 0 || ks > 0) ? 1u : 0u);
+                      st ? dv[kStagesV - 1][ks] : dv[0][ks], kIdescO,
+                      (blk > 0 || ks > 0) ? 1u : 0u);
         }
         if (last) mma_commit(&bar_o[t]);
       };
