@@ -117,9 +117,14 @@ def test_zero_length_chunks_in_the_batch(D):
     _check(w, out, seqs=[s for s in range(w.num_prefill) if chunks[s] > 0])
 
 
-def test_never_written_slots_past_the_end_do_not_leak():
-    # fill everything past each sequence's last token with NaN bit patterns
-    w = W.make_mixed("prefill_nan_tail", 1234, [30], [5, 70], [50, 27], 32, 8, 128, 32)
+@pytest.mark.parametrize("D,P", [(128, 16), (128, 32), (128, 64), (128, 128), (64, 32), (64, 128)])
+def test_never_written_slots_past_the_end_do_not_leak(D, P):
+    # fill everything past each sequence's last token with NaN bit patterns;
+    # the ends fall inside a page, at a page edge inside a 128-key block and
+    # just past a block edge (the last K/V block's tail rows are zeroed before
+    # the PV product reads them)
+    w = W.make_mixed(f"prefill_nan_tail_D{D}_P{P}", 1234 + D + P, [30], [5, 70, 129, 16],
+                     [50, 27, 300, 112], 32, 8, D, P)
     d = device_step_inputs(w)
     kp, vp = device_pools(w)
     P = w.block_size
