@@ -296,7 +296,9 @@ def run_reference(args):
         return 0
     w = _workload(args.workload, args.num_seqs)
     _l2_plan(w, args)
-    seqs = _sample_seqs(w, args.ref_sample_s)
+    # each step's sample is sized so that the whole run (warm-up and timed
+    # steps) takes about 90 s of oracle work at most, whatever --steps is
+    seqs = _sample_seqs(w, min(args.ref_sample_s, 90.0 / max(1, args.steps + args.warmup)))
     inp = _oracle_sample(w, seqs, "cpu")
     for _ in range(args.warmup):
         _oracle_step(w, inp)
@@ -893,7 +895,9 @@ def main(argv=None):
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="keep only the first N sequences (a smaller case, for profiling)")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
-    ap.add_argument("--ref-sample-s", type=float, default=0.5)
+    ap.add_argument("--ref-sample-s", type=float, default=0.5,
+                    help="oracle seconds per step of --impl reference at most (less when "
+                         "steps x that would exceed about 90 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="measure only --workload (by default every other configuration, and "
