@@ -298,6 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStagesK = Lay::kStagesK, kStagesV = Lay::kStagesV;
   constexpr int kOffQ = Lay::kOffQ, kOffK = Lay::kOffK, kOffV = Lay::kOffV;
   constexpr int kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffRank = Lay::kOffRank;
+  if (threadIdx.x == 32 * kKLoadWarp) {  // the loaders' tensor maps, fetched ahead of their first copies
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+  }
   pdl_wait();  // inputs written by earlier kernels of the stream are visible
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
