@@ -83,6 +83,28 @@ def oracle_prefill_rows(w: W.Workload, s: int, h: int, kv_new_h=None):
     return out
 
 
+def oracle_prefill_window(w: W.Workload, s: int, h: int, r0: int, r1: int, kv_new_h=None):
+    """fp64 oracle output [r1 - r0, G, D] of rows r0 .. r1-1 of prefill
+    sequence s's chunk, q heads of kv head h: those rows are the last r1 - r0
+    tokens of the same sequence cut at length L - C + r1, so the oracle runs
+    on that shorter sequence (its first pages, the window's q rows)."""
+    L = int(w.prefill_context_lens[s])
+    C = int(w.prefill_chunk_lens[s])
+    assert 0 <= r0 < r1 <= C
+    Lw = L - C + r1
+    P = w.block_size
+    npg = (Lw + P - 1) // P
+    pages = w.prefill_block_tables[s, :npg]
+    kp, vp = host_head_pools(w, pages, h, *(kv_new_h or (None, None)))
+    G = w.group
+    cu = w.cu_seqlens_q()
+    q = W.bf16_bits(w.q_prefill()[cu[s] + r0:cu[s] + r1, h * G:(h + 1) * G, :])
+    table = np.arange(max(npg, 1), dtype=np.int32)[None]
+    ks, vs = w.head_scales(h)
+    return oracle.paged_prefill(q, np.array([0, r1 - r0], np.int32), kp, vp, table,
+                                np.array([Lw], np.int32), w.scale, w.kv_dtype, ks, vs)
+
+
 def assert_close(got_bf16: torch.Tensor, want: np.ndarray, fp8: bool, what=""):
     got = got_bf16.detach().float().cpu().numpy().astype(np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)

@@ -12,7 +12,7 @@ import torch
 import paged_kv_attention_31_gb300 as pkv
 import workloads as W
 from tests._gpu_state import (assert_close, device_pools, device_step_inputs,
-                              oracle_decode_rows, oracle_prefill_rows)
+                              oracle_decode_rows, oracle_prefill_rows, oracle_prefill_window)
 
 pytestmark = pytest.mark.gpu
 
@@ -203,6 +203,29 @@ def test_full_size_mixed_step_sampled():
         h = int(rng.integers(0, w.num_kv_heads))
         assert_close(out_d[s, h * G:(h + 1) * G], oracle_decode_rows(w, s, h), False,
                      f"mixed decode s={s}")
+
+
+def test_full_size_long_context_prefill_sampled():
+    # 8 chunks of 1024 onto prior contexts of 4096 (the benchmark's long-context
+    # case): 1024 CTAs in several waves, up to 40 key blocks per tile; 32-row
+    # windows at each sampled chunk's start, middle and end against the oracle
+    w = W.config("long_prefill")
+    d = device_step_inputs(w)
+    kp, vp = device_pools(w)
+    out = _prefill(w, d, kp, vp)
+    assert pkv.get_device_error() == 0
+    G = w.group
+    cu = w.cu_seqlens_q()
+    kn, vn = w.kv_new()
+    rng = np.random.default_rng(31)
+    for s in (0, 3, w.num_prefill - 1):
+        h = int(rng.integers(0, w.num_kv_heads))
+        kv = (W.bf16_bits(kn[:, h, :]), W.bf16_bits(vn[:, h, :]))
+        C = int(w.prefill_chunk_lens[s])
+        for r0 in (0, C // 2 - 16, C - 32):
+            want = oracle_prefill_window(w, s, h, r0, r0 + 32, kv)
+            assert_close(out[cu[s] + r0:cu[s] + r0 + 32, h * G:(h + 1) * G], want, False,
+                         f"{w.name} s={s} h={h} rows {r0}..{r0 + 31}")
 
 
 # ---- FP8 pools -------------------------------------------------------------------
